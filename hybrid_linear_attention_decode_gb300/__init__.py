@@ -1,0 +1,171 @@
+"""GB300-native (sm_103a) Kimi Delta Attention serving hot path -- Python binding of ``libkda.so``.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels behind the C ABI declared in
+``include/kda.h``.  PyTorch provides device memory and streams.  There is no fallback: if the library
+is missing the import of an entry point raises.
+
+Entry points (same names as the C ABI): ``kda_decode_step``, ``kda_prefill_chunked``,
+``kda_resume_from_slot``, ``kda_prefill_workspace_bytes``, ``kda_checkpoint_count``,
+``kda_status_string``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+_lib = None
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED_SHAPE, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = 0, 1, 2, 3, 4
+KDA_DEV_BAD_SLOT, KDA_DEV_BAD_SEQLENS, KDA_DEV_BAD_CKPT, KDA_DEV_DECAY_RANGE, KDA_DEV_TIMEOUT = 1, 2, 4, 8, 16
+
+
+class KdaError(RuntimeError):
+    def __init__(self, rc: int, what: str):
+        super().__init__(f"{what}: {kda_status_string(rc)} (status {rc})")
+        self.rc = rc
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("conv_w", ctypes.c_int32),
+                ("num_slots", ctypes.c_int64), ("S", ctypes.c_void_p), ("conv", ctypes.c_void_p)]
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("conv_weight", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p), ("l2_eps", ctypes.c_float),
+                ("rms_eps", ctypes.c_float), ("scale", ctypes.c_float), ("conv_silu", ctypes.c_int32)]
+
+
+def load_library(path: str | None = None):
+    """Load libkda.so (built in-tree by ``hybrid_linear_attention_decode_gb300/build.py``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libkda.so not built ({p}); run __graft_entry__.build() first")
+    lib = ctypes.CDLL(p)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.kda_decode_step.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Params), i32] + [vp] * 11
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_checkpoint_count.argtypes = [i64, i64, i64]
+    lib.kda_checkpoint_count.restype = i64
+    lib.kda_prefill_workspace_bytes.argtypes = [ctypes.POINTER(_Pool), i32, i64, i32]
+    lib.kda_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.kda_prefill_chunked.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Params), i32, i64, vp, vp, vp, vp, i32,
+                                        i64, vp, vp] + [vp] * 7 + [vp, ctypes.c_size_t, vp, vp]
+    lib.kda_prefill_chunked.restype = ctypes.c_int
+    lib.kda_resume_from_slot.argtypes = [ctypes.POINTER(_Pool), i32, vp, vp, vp, vp]
+    lib.kda_resume_from_slot.restype = ctypes.c_int
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_version.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libkda must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclass
+class StatePool:
+    """The state-slot pool: S [num_slots, H, dk, dv] fp32 and conv [num_slots, H, W-1, 2dk+dv] bf16."""
+    S: torch.Tensor
+    conv: torch.Tensor
+
+    @staticmethod
+    def empty(num_slots: int, H: int, dk: int, dv: int, W: int = 4, device="cuda") -> "StatePool":
+        return StatePool(torch.zeros(num_slots, H, dk, dv, dtype=torch.float32, device=device),
+                         torch.zeros(num_slots, H, W - 1, 2 * dk + dv, dtype=torch.bfloat16, device=device))
+
+    def c(self) -> _Pool:
+        ns, H, dk, dv = self.S.shape
+        return _Pool(H, dk, dv, self.conv.shape[2] + 1, ns, _ptr(self.S), _ptr(self.conv))
+
+
+@dataclass
+class LayerParams:
+    """conv_weight [H, 2dk+dv, W] fp32, norm_weight [dv] fp32 and the layer's constants."""
+    conv_weight: torch.Tensor
+    norm_weight: torch.Tensor
+    l2_eps: float = 1e-6
+    rms_eps: float = 1e-6
+    scale: float = 1.0
+    conv_silu: bool = True
+
+    def c(self) -> _Params:
+        return _Params(_ptr(self.conv_weight), _ptr(self.norm_weight), self.l2_eps, self.rms_eps, self.scale,
+                       int(bool(self.conv_silu)))
+
+
+def kda_status_string(rc: int) -> str:
+    return load_library().kda_status_string(int(rc)).decode()
+
+
+def kda_checkpoint_count(start_pos: int, length: int, interval: int) -> int:
+    return int(load_library().kda_checkpoint_count(int(start_pos), int(length), int(interval)))
+
+
+def kda_prefill_workspace_bytes(pool: StatePool, nseq: int, total_tokens: int, chunk: int) -> int:
+    pc = pool.c()
+    return int(load_library().kda_prefill_workspace_bytes(ctypes.byref(pc), int(nseq), int(total_tokens), int(chunk)))
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != KDA_OK:
+        raise KdaError(rc, what)
+
+
+def kda_decode_step(pool: StatePool, params: LayerParams, q, k, v, a, b, z, y, src_slot, dst_slot, dev_status,
+                    stream=None) -> None:
+    """One fused decode token per request; see include/kda.h.  Tensors: q,k,a [n,H,dk] bf16, v,z,y
+    [n,H,dv] bf16, b [n,H] bf16, src_slot/dst_slot [n] int32, dev_status [1] int32 (all on the GPU)."""
+    n = int(src_slot.shape[0])
+    pc, pp = pool.c(), params.c()
+    rc = load_library().kda_decode_step(ctypes.byref(pc), ctypes.byref(pp), n, _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                        _ptr(b), _ptr(z), _ptr(y), _ptr(src_slot), _ptr(dst_slot),
+                                        _ptr(dev_status), _stream(stream))
+    _check(rc, "kda_decode_step")
+
+
+def kda_prefill_chunked(pool: StatePool, params: LayerParams, cu_seqlens, start_pos, src_slot, dst_slot, chunk: int,
+                        ckpt_interval: int, ckpt_offsets, ckpt_slots, q, k, v, a, b, z, y, workspace, dev_status,
+                        stream=None) -> None:
+    """Chunked prefill with checkpoint emission; see include/kda.h.  cu_seqlens/ckpt_offsets int32
+    [nseq+1], start_pos int64 [nseq], slots int32, workspace a uint8 tensor of
+    kda_prefill_workspace_bytes() bytes."""
+    nseq = int(start_pos.shape[0])
+    T = int(q.shape[0]) if q is not None else 0
+    pc, pp = pool.c(), params.c()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load_library().kda_prefill_chunked(
+        ctypes.byref(pc), ctypes.byref(pp), nseq, T, _ptr(cu_seqlens), _ptr(start_pos), _ptr(src_slot),
+        _ptr(dst_slot), int(chunk), int(ckpt_interval), _ptr(ckpt_offsets), _ptr(ckpt_slots), _ptr(q), _ptr(k),
+        _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(y), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(rc, "kda_prefill_chunked")
+
+
+def kda_resume_from_slot(pool: StatePool, src_slot, dst_slot, dev_status, stream=None) -> None:
+    """Copy-on-write: slot dst_slot[i] receives a bit-exact copy of slot src_slot[i] (int32 [n])."""
+    pc = pool.c()
+    rc = load_library().kda_resume_from_slot(ctypes.byref(pc), int(src_slot.shape[0]), _ptr(src_slot),
+                                             _ptr(dst_slot), _ptr(dev_status), _stream(stream))
+    _check(rc, "kda_resume_from_slot")

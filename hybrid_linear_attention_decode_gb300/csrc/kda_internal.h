@@ -1,0 +1,71 @@
+// kda_internal.h -- launcher interfaces between the C-ABI layer (kda_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+struct DecodeArgs {
+    float *S;            // pool states [num_slots][H][dk][dv]
+    uint16_t *conv;      // pool windows [num_slots][H][W-1][2dk+dv]
+    int64_t num_slots;
+    int32_t H, n;
+    const float *conv_w, *norm_w;
+    float l2_eps, rms_eps, scale;
+    int32_t silu;
+    const uint16_t *q, *k, *v, *a, *b, *z;
+    uint16_t *y;
+    const int32_t *src, *dst;
+    int32_t *status;
+};
+
+struct ResumeArgs {
+    float *S;
+    uint16_t *conv;
+    int64_t num_slots;
+    int32_t H, n;
+    int32_t s_words16;     // 16-byte words per (slot, head) state
+    int32_t conv_words16;  // 16-byte words per (slot, head) window
+    const int32_t *src, *dst;
+    int32_t *status;
+};
+
+struct PrefillArgs {
+    float *S;
+    uint16_t *conv;
+    int64_t num_slots;
+    int32_t H, nseq;
+    int64_t total_tokens;
+    const float *conv_w, *norm_w;
+    float l2_eps, rms_eps, scale;
+    int32_t silu;
+    const int32_t *cu_seqlens;
+    const int64_t *start_pos;
+    const int32_t *src, *dst;
+    int32_t chunk;
+    int64_t interval;
+    const int32_t *ckpt_offsets, *ckpt_slots;
+    const uint16_t *q, *k, *v, *a, *b, *z;
+    uint16_t *y;
+    void *ws;
+    size_t ws_bytes;
+    int32_t *status;
+};
+
+bool decode_supported(int dk, int dv, int W);
+int launch_decode(const DecodeArgs &a, int dk, int dv, cudaStream_t st);
+
+int launch_resume(const ResumeArgs &a, cudaStream_t st);
+
+bool prefill_supported(int dk, int dv, int W, int chunk);
+size_t prefill_workspace_bytes(int H, int dk, int dv, int nseq, int64_t total_tokens, int chunk);
+int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st);
+
+// Streaming multiprocessors of the current device (cached per device).
+int current_device_sms();
+
+}  // namespace kda

@@ -1,0 +1,173 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention (KDA) serving hot path.
+ *
+ * KDA is the gated delta rule with channel-wise decay used by Kimi Linear / Kimi K3:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T ,   o_t = scale * S_t^T q_t
+ *
+ * Per request and head it keeps a dk x dv fp32 recurrent state S and a short causal-convolution state
+ * ("A Preview of Production-Scale Kimi K3 Support on vLLM", section "The Hardest Part: Prefix Caching
+ * for KDA": each KDA layer advances a matrix-like recurrent state together with a short convolution
+ * state).  One token, for one head, is processed as:
+ *   1. causal conv of width W over the raw q | k | v channels (weights [H][2dk+dv][W], tap W-1 on the
+ *      current input, tap 0 on the oldest stored one), then SiLU when conv_silu != 0;
+ *   2. q^ = q / sqrt(|q|^2 + l2_eps), k^ likewise (v is the conv output as is);
+ *   3. alpha = sigmoid(a) per key channel, beta = sigmoid(b) per head (a, b are logits);
+ *   4. the update above;  5. o = scale * S^T q^;
+ *   6. y = o / sqrt(mean(o^2) + rms_eps) * norm_weight * sigmoid(z)   (gate factor 1 when z is NULL).
+ *
+ * All entry points are asynchronous on the given stream, allocate nothing, keep no state between
+ * calls, and never synchronise the host, so they may be captured in a CUDA graph.  The caller owns
+ * every buffer.  All pointers named "device" must be device (or managed) memory of the current device,
+ * 16-byte aligned.  bf16 tensors are passed as their uint16 bit patterns.
+ *
+ * Errors: problems visible on the host return a kda_status before anything is launched.  Problems only
+ * visible on the device (an out-of-range slot index, inconsistent sequence or checkpoint tables, a
+ * decay logit outside the chunked form's range) OR a bit into *dev_status (a device int32 the caller
+ * zeroes and reads after synchronising) and skip the affected work item; kernels never trap.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+/* Same type as cudaStream_t.  NULL is the legacy default stream. */
+typedef struct CUstream_st *kda_stream_t;
+
+/* Host-side return codes. */
+enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,       /* NULL pointer, negative count, misaligned pointer, bad interval */
+    KDA_ERR_UNSUPPORTED_SHAPE = 2, /* (dk, dv, conv width, chunk) not compiled in */
+    KDA_ERR_WORKSPACE = 3,         /* workspace NULL or smaller than kda_prefill_workspace_bytes() */
+    KDA_ERR_CUDA = 4               /* a CUDA launch or attribute call failed */
+};
+
+/* Device-side status bits, OR-ed into *dev_status. */
+#define KDA_DEV_BAD_SLOT 0x1      /* a slot index outside [0, num_slots) (src may also be -1) */
+#define KDA_DEV_BAD_SEQLENS 0x2   /* cu_seqlens not non-decreasing from 0 to total_tokens, or start_pos < 0 */
+#define KDA_DEV_BAD_CKPT 0x4      /* ckpt_offsets does not give sequence n exactly its boundary count */
+#define KDA_DEV_DECAY_RANGE 0x8   /* prefill: a decay logit below -KDA_MIN_DECAY_LOGIT's range (see below) */
+#define KDA_DEV_TIMEOUT 0x10      /* a bounded wait on an asynchronous copy gave up */
+
+/*
+ * Chunked prefill evaluates exp(+-cumulative log-decay) over half a 16-token sub-block; to stay inside
+ * fp32 range each per-token decay logit must satisfy a >= KDA_MIN_DECAY_LOGIT (alpha >= ~4.5e-5).
+ * Tokens below it set KDA_DEV_DECAY_RANGE.  Decode has no such limit.
+ */
+#define KDA_MIN_DECAY_LOGIT (-10.0f)
+
+/*
+ * The state-slot pool ("The Hardest Part: Prefix Caching for KDA": the physical state block is
+ * decoupled from the prefix-match unit; a slot here is one state snapshot).  Layout, slot-major:
+ *   S    [num_slots][H][dk][dv]         fp32, row i = key channel, column j = value channel
+ *   conv [num_slots][H][W-1][2dk+dv]    bf16, the last W-1 RAW (pre-conv) q|k|v inputs, oldest first
+ * Both device, owned by the caller.
+ */
+typedef struct kda_pool {
+    int32_t H, dk, dv, conv_w;  /* heads, key dim, value dim, conv width W */
+    int64_t num_slots;
+    float *S;
+    uint16_t *conv;
+} kda_pool;
+
+/* Layer constants. */
+typedef struct kda_params {
+    const float *conv_weight; /* device [H][2dk+dv][W] fp32 */
+    const float *norm_weight; /* device [dv] fp32 (shared by all heads) */
+    float l2_eps;             /* q/k normalisation: x / sqrt(|x|^2 + l2_eps) */
+    float rms_eps;            /* output RMSNorm epsilon */
+    float scale;              /* readout scale */
+    int32_t conv_silu;        /* 1: SiLU after the conv; 0: none */
+} kda_params;
+
+/*
+ * One decode token for each of n requests, all heads, in one launch: conv, gates, state update,
+ * readout and gated RMSNorm fused ("A Preview of Production-Scale Kimi K3 Support on vLLM", section
+ * "KDA prefill and decode"; "vLLM Kimi K3 Support", section "Fused Kernels and Metadata Optimization":
+ * one launch, no intermediate tensors, no repeated state traffic).
+ *   q, k      device [n][H][dk] bf16        v, z  device [n][H][dv] bf16 (z may be NULL: no gate)
+ *   a         device [n][H][dk] bf16 (decay logits)   b  device [n][H] bf16 (beta logits)
+ *   y         device [n][H][dv] bf16 output
+ *   src_slot  device [n] int32: state read from this slot; -1 = fresh request (zero state and window)
+ *   dst_slot  device [n] int32: updated state and window written here (src == dst: in place)
+ *   dev_status device int32, OR-ed with KDA_DEV_* bits.
+ * Within one call no dst slot may repeat and no slot may be the src of one request and the dst of
+ * another ("The Hardest Part: Prefix Caching for KDA": same-step reuse is deferred until the copy is
+ * safe).  A request with a bad slot index gets y = 0 and no state write.
+ * Supported: (dk, dv) in {(16,16), (32,16), (16,32), (64,64), (128,128)}, W = 4.
+ */
+KDA_API int kda_decode_step(const kda_pool *pool, const kda_params *prm, int32_t n, const uint16_t *q, const uint16_t *k,
+                    const uint16_t *v, const uint16_t *a, const uint16_t *b, const uint16_t *z, uint16_t *y,
+                    const int32_t *src_slot, const int32_t *dst_slot, int32_t *dev_status, kda_stream_t stream);
+
+/*
+ * Checkpoint boundaries of one sequence: the prefix lengths p with p % interval == 0 and
+ * start_pos < p <= start_pos + len ("vLLM Kimi K3 Support", section "Agentic Cache Retention Policies":
+ * interval-based retention; "moonshotai/Kimi-K3" recipe: prefix-match unit 128).  Host function; returns
+ * the count (0 when interval <= 0 or len <= 0), or -1 for start_pos < 0.
+ */
+KDA_API int64_t kda_checkpoint_count(int64_t start_pos, int64_t len, int64_t interval);
+
+/* Bytes of device workspace kda_prefill_chunked needs for these sizes (host function, no CUDA call). */
+KDA_API size_t kda_prefill_workspace_bytes(const kda_pool *pool, int32_t nseq, int64_t total_tokens, int32_t chunk);
+
+/*
+ * Chunked prefill of nseq variable-length sequences with checkpoint emission into the pool ("A Preview
+ * of Production-Scale Kimi K3 Support on vLLM", sections "KDA prefill and decode" -- chunked prefill and
+ * one-operation initial-state gather -- and "The Hardest Part: Prefix Caching for KDA" -- the state
+ * must exist at the exact prefix boundary).
+ *   cu_seqlens  device [nseq+1] int32, cu_seqlens[0] = 0, non-decreasing, cu_seqlens[nseq] = total_tokens
+ *   start_pos   device [nseq] int64: absolute position of each sequence's first token (tokens already
+ *               in its state); chunks are aligned to absolute positions, so a resumed sequence
+ *               computes exactly what a full replay computes from the same boundary on
+ *   src_slot, dst_slot  as for decode (src -1 = empty prefix)
+ *   chunk       tokens per chunk (16 or 64)
+ *   ckpt_interval  0 = no checkpoints; else a positive multiple of chunk
+ *   ckpt_offsets   device [nseq+1] int32: sequence n's boundaries (kda_checkpoint_count of them,
+ *               ascending) own entries ckpt_offsets[n] .. ckpt_offsets[n+1]-1 of ckpt_slots
+ *   ckpt_slots     device int32: slot receiving (S, conv window) at that boundary, or -1 to skip.
+ *               A boundary equal to the sequence end is emitted too.
+ *   q,k,v,a,b,z,y  as for decode with n replaced by total_tokens (token-major)
+ *   workspace   device, at least kda_prefill_workspace_bytes() bytes, contents need not be initialised
+ * Same aliasing rules as decode, with checkpoint slots counting as dst slots.
+ * Supported: (dk, dv) as for decode, W = 4, chunk in {16, 64}.
+ */
+KDA_API int kda_prefill_chunked(const kda_pool *pool, const kda_params *prm, int32_t nseq, int64_t total_tokens,
+                        const int32_t *cu_seqlens, const int64_t *start_pos, const int32_t *src_slot,
+                        const int32_t *dst_slot, int32_t chunk, int64_t ckpt_interval, const int32_t *ckpt_offsets,
+                        const int32_t *ckpt_slots, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const uint16_t *a, const uint16_t *b, const uint16_t *z, uint16_t *y, void *workspace,
+                        size_t workspace_bytes, int32_t *dev_status, kda_stream_t stream);
+
+/*
+ * Copy-on-write resume ("The Hardest Part: Prefix Caching for KDA": a cached partial state is copied
+ * into a private destination before the request extends it): for each of n pairs, slot dst_slot[i]
+ * receives a bit-exact copy of slot src_slot[i] (state and conv window, all heads).  src_slot and
+ * dst_slot are device [n] int32; dst slots must be distinct and must not be src slots of the same call.
+ */
+KDA_API int kda_resume_from_slot(const kda_pool *pool, int32_t n, const int32_t *src_slot, const int32_t *dst_slot,
+                         int32_t *dev_status, kda_stream_t stream);
+
+/* Static description of a kda_status value. */
+KDA_API const char *kda_status_string(int status);
+
+/* Library version, for the loader's sanity check. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

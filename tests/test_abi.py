@@ -1,0 +1,91 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point include/kda.h declares;
+host-side argument checks work without a GPU (no kernel is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from hybrid_linear_attention_decode_gb300 import build as kbuild
+    import hybrid_linear_attention_decode_gb300 as kda
+    kbuild.build()
+    return kda.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    return re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", src)
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("kda_decode_step", "kda_prefill_chunked", "kda_resume_from_slot"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    import hybrid_linear_attention_decode_gb300 as kda
+    assert lib.kda_version() >= 1
+    assert kda.kda_status_string(0) == "ok"
+    for rc in range(1, 5):
+        assert kda.kda_status_string(rc) != "unknown status"
+
+
+def test_checkpoint_count_matches_the_oracle(lib):
+    import oracle
+    import hybrid_linear_attention_decode_gb300 as kda
+    for start in (0, 1, 31, 32, 127, 128, 32768):
+        for length in (0, 1, 31, 32, 33, 1024):
+            for interval in (0, 16, 32, 128, 32768):
+                exp = oracle.ckpt_count(start, length, interval) if interval > 0 else 0
+                assert kda.kda_checkpoint_count(start, length, interval) == exp
+    assert kda.kda_checkpoint_count(-1, 4, 2) == -1
+
+
+def test_host_validation_without_gpu(lib):
+    import hybrid_linear_attention_decode_gb300 as kda
+    # NULL pool / params: rejected before any CUDA call
+    assert lib.kda_decode_step(None, None, 1, *([None] * 11)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_resume_from_slot(None, 1, None, None, None, None) == kda.KDA_ERR_INVALID_ARG
+    pool = kda._Pool(2, 128, 128, 4, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
+    # unsupported shape / misaligned pointers are host errors
+    bad = kda._Pool(2, 96, 128, 4, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
+    prm = kda._Params(ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000), 1e-6, 1e-6, 1.0, 1)
+    assert lib.kda_decode_step(ctypes.byref(bad), ctypes.byref(prm), 1, *([None] * 11)) == \
+        kda.KDA_ERR_UNSUPPORTED_SHAPE
+    mis = kda._Pool(2, 128, 128, 4, 8, ctypes.c_void_p(0x1004), ctypes.c_void_p(0x2000))
+    assert lib.kda_decode_step(ctypes.byref(mis), ctypes.byref(prm), 1, *([None] * 11)) == kda.KDA_ERR_INVALID_ARG
+    # n = 0 is a no-op that returns OK without touching the device
+    assert lib.kda_decode_step(ctypes.byref(pool), ctypes.byref(prm), 0, *([None] * 11)) == kda.KDA_OK
+    assert lib.kda_resume_from_slot(ctypes.byref(pool), 0, None, None, None, None) == kda.KDA_OK
+
+
+def test_product_package_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "hybrid_linear_attention_decode_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower() or f.endswith(".md"), f
+
+
+def test_binding_argument_counts_match_header(lib):
+    """The ctypes signatures declare exactly the parameters include/kda.h gives each entry point."""
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    for name in declared_functions():
+        m = re.search(r"KDA_API[^;(]*\b" + name + r"\s*\(([^)]*)\)", src)
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        argtypes = getattr(lib, name).argtypes or []
+        assert len(argtypes) == len(params), (name, len(argtypes), len(params))
