@@ -1,0 +1,497 @@
+"""Benchmark of the KDA serving hot path on GB300.
+
+Prints ONE JSON line (rank 0).  Workload: the decode step (batch 64 requests, H=32, dk=dv=128, conv
+width 4, fp32 states in a 4096-slot pool, a fresh random draw of 64 distinct slots every step, in place).
+`value` = decode tokens/s over all ranks, with inputs resident in HBM; `e2e` = the same through the
+C-ABI call with the step's token inputs copied from pinned host memory and y copied back inside the
+timed region.  `prefill` adds the chunked-prefill workload (4 sequences of 2048/4096/8192/8192 tokens,
+chunk 64, checkpoints every 128 tokens into pool slots) timed the same way.  `cpu_baseline` times the
+fp64 oracle on this host's cores on a bounded sample of the decode workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Multi-GPU (weak scaling, one independent batch per rank, no collective on the data path):
+  python -m torch.distributed.run --nproc-per-node N --master-addr 127.0.0.1 ... bench.py --gpus N
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import kda_inputs as ki  # noqa: E402
+
+METRIC = "KDA decode tokens/s + state GB/s vs HBM peak; chunked-prefill tokens/s"
+H, DK, DV, W = 32, 128, 128, 4
+DEC_N, DEC_SLOTS = 64, 4096
+PRE_LENS, PRE_CHUNK, PRE_INTERVAL = (2048, 4096, 8192, 8192), 64, 128
+DECODE_BYTES_PER_HEAD_TOKEN = 2 * DK * DV * 4 + 2 * (W - 1) * (2 * DK + DV) * 2 + (3 * DK + DK + DV + DV) * 2 + 2
+PREFILL_IO_BYTES_PER_HEAD_TOKEN = (2 * DK + DV + DK + DV + DV) * 2 + 2
+CKPT_BYTES = DK * DV * 4 + (W - 1) * (2 * DK + DV) * 2
+
+
+# ----------------------------------------------------------------------------- multi-rank plumbing
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    """Slowest rank's value (the whole job is as slow as its slowest rank)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank serves an independent batch (weak scaling)."""
+    return base + 7919 * rank
+
+
+# ----------------------------------------------------------------------------- peaks and clocks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0) or 0), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while a region runs."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + ",".join(self.FIELDS),
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def file_sha(*paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name: str, sha: str):
+    """dram bytes per launch recorded in profiles/<name>_traffic.txt for this exact kernel source, else None."""
+    path = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha") == sha:
+            return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle (baseline / reference)
+class OracleDecodeSample:
+    """One decode step of the fp64 oracle for a sample of n requests (all heads) of the decode workload."""
+
+    def __init__(self, n: int, seed: int = 2):
+        import oracle
+        oracle.build()
+        self.oracle, self.n = oracle, n
+        self.cfg = oracle.Cfg(H=H, dk=DK, dv=DV, W=W)
+        self.wts = ki.layer_weights(seed, H, DK, DV, W)
+        tok = ki.token_inputs(seed, n, H, DK, DV)
+        self.f = {k: ki.bf16_bits_to_f64(v) for k, v in tok.items()}
+        S_h, C_h = ki.pool_tiles(seed, H, DK, DV, W, np.arange(n * H))
+        self.S0 = S_h.reshape(n, H, DK, DV).astype(np.float64)
+        self.C0 = ki.bf16_bits_to_f64(C_h).reshape(n, H, W - 1, 2 * DK + DV)
+        self.cu, self.sp = np.arange(n + 1), np.zeros(n, dtype=np.int64)
+
+    def step(self) -> float:
+        f = self.f
+        t0 = time.perf_counter()
+        self.oracle.forward(self.cfg, self.cu, self.sp, f["q"], f["k"], f["v"], f["a"], f["b"], f["z"],
+                            self.wts["conv_w"], self.wts["norm_w"], self.S0, self.C0)
+        return time.perf_counter() - t0
+
+
+def oracle_decode_rate(seconds: float, seed: int = 2) -> dict:
+    """fp64 oracle on this host: repeated decode steps of 16 of the 64 requests, for about `seconds`."""
+    smp = OracleDecodeSample(16, seed)
+    reps, dt = 0, 0.0
+    while dt < seconds:
+        dt += smp.step()
+        reps += 1
+    return {"value": reps * smp.n / dt, "unit": "tokens/s", "cores": smp.oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} repetitions of one decode step for {smp.n} of the 64 requests (all {H} heads, "
+                      f"dk=dv={DK}, 4096-slot pool contents), fp64, {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle as it stands, timed on this host's cores, each step one oracle
+    decode call on a sample of the decode workload sized so that the whole run takes a few minutes."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    probe = OracleDecodeSample(16)
+    t16 = min(probe.step() for _ in range(3))
+    total = args.steps + args.warmup
+    n = 16 if total * t16 <= 150.0 else max(1, int(16 * 150.0 / (total * t16)))
+    smp = probe if n == 16 else OracleDecodeSample(n)
+    for _ in range(args.warmup):
+        smp.step()
+    dt = sum(smp.step() for _ in range(args.steps))
+    val = args.steps * n / dt
+    sample = (f"each step: one fp64 oracle decode step for {n} of the 64 requests (all {H} heads, dk=dv={DK}); "
+              f"{args.steps} steps in {dt:.1f} s")
+    line = {"metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "decode step: batch 64 requests, H=32, dk=dv=128, conv width 4, 4096-slot "
+                                   "pool (bounded sample per step, see cpu_baseline)"},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": smp.oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def bf16_dev(bits, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def run_gpu(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    import hybrid_linear_attention_decode_gb300 as kda
+    try:
+        kda.load_library()
+    except RuntimeError:
+        from hybrid_linear_attention_decode_gb300 import build as kbuild
+        kbuild.build()
+        kda.load_library()
+    hbm_peak, _, _, peak_kind = measured_peaks()
+    seed = rank_seed(2, rank)
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- decode workload
+    pool = kda.StatePool.empty(DEC_SLOTS, H, DK, DV, W, device=dev)
+    ki.fill_device_pool(pool.S, pool.conv, seed)
+    wts = ki.layer_weights(seed, H, DK, DV, W)
+    prm = kda.LayerParams(torch.from_numpy(wts["conv_w"]).to(dev), torch.from_numpy(wts["norm_w"]).to(dev))
+    tok = ki.token_inputs(seed, DEC_N, H, DK, DV)
+    d = {k: bf16_dev(v, dev) for k, v in tok.items()}
+    y = torch.empty(DEC_N, H, DV, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    K, Wm = args.steps, args.warmup
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    nd = Wm + K
+    slots = torch.rand(nd, DEC_SLOTS, device=dev, generator=g).argsort(dim=1)[:, :DEC_N].to(torch.int32).contiguous()
+
+    def dec(i, st=stream):
+        s = slots[i % nd]
+        kda.kda_decode_step(pool, prm, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y, s, s, status, st)
+
+    for i in range(Wm):
+        dec(i)
+    torch.cuda.synchronize()
+    # per-launch kernel time from events around eager launches (diagnostic)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for i, (a, b) in enumerate(ev):
+        a.record(stream)
+        dec(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    eager_launch_ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+    # the timed region: one replay of a captured graph of exactly K decode steps (fresh slots per step)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(K):
+            dec(Wm + i, None)
+    graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    region_ms = start.elapsed_time(end)
+    launch_ms = region_ms / K
+    # keep the GPU busy (untimed) until the sampler has seen over a second of load
+    while time.time() - t_wall0 < 1.5:
+        graph.replay()
+        torch.cuda.synchronize()
+    t_wall2 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall2)
+    del graph
+    assert int(status.item()) == 0, f"decode status {int(status.item())}"
+    region_ms = max_over_ranks(region_ms, ws)
+    dec_tokens = DEC_N * ws
+    value = dec_tokens * K / (region_ms / 1000.0)
+    bytes_per_launch = DECODE_BYTES_PER_HEAD_TOKEN * DEC_N * H
+    achieved = bytes_per_launch / (launch_ms / 1000.0) / 1e9
+    state_gbs = 2 * DK * DV * 4 * DEC_N * H / (launch_ms / 1000.0) / 1e9
+    dec_sha = file_sha("hybrid_linear_attention_decode_gb300/csrc/kda_decode.cu",
+                       "hybrid_linear_attention_decode_gb300/csrc/kda_device.cuh")
+    traffic = profiled_traffic("kda_decode", dec_sha)
+
+    # ---- end to end through the C ABI: token inputs from pinned host memory, y back to the host
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
+               for k, v in tok.items()}
+    host_slots = slots.cpu().pin_memory()
+    host_y = torch.empty(DEC_N, H, DV, dtype=torch.bfloat16).pin_memory()
+    dev_slots = torch.empty(DEC_N, dtype=torch.int32, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + DEC_N * 4
+    d2h = host_y.numel() * host_y.element_size()
+
+    def e2e_step(i):
+        for k_, t in host_in.items():
+            d[k_].copy_(t, non_blocking=True)
+        dev_slots.copy_(host_slots[i % nd], non_blocking=True)
+        kda.kda_decode_step(pool, prm, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y, dev_slots, dev_slots,
+                            status, stream)
+        host_y.copy_(y, non_blocking=True)
+
+    for i in range(Wm):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        e2e_step(Wm + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    e2e_val = dec_tokens * K / (e2e_ms / 1000.0)
+
+    # ---- chunked prefill workload
+    prefill = run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+            "ms_per_step": region_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp32", "data": "synthetic",
+            "config": {"workload": "decode step: batch 64 requests, H=32, dk=dv=128, conv width 4, fp32 state "
+                                   "pool of 4096 slots (8 GiB), 64 distinct random slots per step, in place",
+                       "global_batch": DEC_N * ws, "per_gpu_batch": DEC_N, "heads": H, "dk": DK, "dv": DV,
+                       "l2": "inputs larger than L2: every step draws fresh random slots from an 8 GiB pool",
+                       "parallelism": f"replicas x{ws} (independent batches per GPU)"},
+            "state_gbs": state_gbs,
+            "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": achieved, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": peak_kind,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
+                         "launch_ms": launch_ms, "eager_launch_ms_median": eager_launch_ms},
+            "clocks": clocks,
+            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": K,
+            "prefill": prefill}
+    if rank == 0:
+        if ws == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_decode_rate(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def prefill_problem(seed: int, lens, chunk: int, interval: int, num_slots: int):
+    """Token inputs, tables and slot plan of a varlen prefill from empty prefixes."""
+    T = int(sum(lens))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    sp = np.zeros(len(lens), dtype=np.int64)
+    counts = [(l // interval) if interval else 0 for l in lens]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    nck = int(offs[-1])
+    perm = ki.permutation(seed, ki.STREAM["slots"] + 77, num_slots)
+    dst = perm[:len(lens)].astype(np.int32)
+    ck = perm[len(lens):len(lens) + nck].astype(np.int32)
+    return T, cu, sp, dst, offs, ck
+
+
+def run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
+    T, cu, sp, dst, offs, ck = prefill_problem(seed, PRE_LENS, PRE_CHUNK, PRE_INTERVAL, DEC_SLOTS)
+    tok = ki.token_inputs(seed + 1, T, H, DK, DV)
+    d = {k: bf16_dev(v, dev) for k, v in tok.items()}
+    y = torch.empty(T, H, DV, dtype=torch.bfloat16, device=dev)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    cu_d, sp_d, dst_d, offs_d, ck_d = t(cu, 0), t(sp, 0), t(dst, 0), t(offs, 0), t(ck, 0)
+    src_d = torch.full((len(PRE_LENS),), -1, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    try:
+        nbytes = kda.kda_prefill_workspace_bytes(pool, len(PRE_LENS), T, PRE_CHUNK)
+        if nbytes == 0:
+            return None
+        ws_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def pre():
+            kda.kda_prefill_chunked(pool, prm, cu_d, sp_d, src_d, dst_d, PRE_CHUNK, PRE_INTERVAL, offs_d, ck_d,
+                                    d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y, ws_buf, status, stream)
+        Kp, Wp = max(3, min(args.steps, 20)), max(3, args.warmup)
+        for _ in range(Wp):
+            pre()
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Kp):
+            pre()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1), ws) / Kp
+    except kda.KdaError as e:
+        return {"error": str(e)}
+    io = PREFILL_IO_BYTES_PER_HEAD_TOKEN * T * H + CKPT_BYTES * int(offs[-1]) * H + len(PRE_LENS) * H * CKPT_BYTES
+    return {"workload": "chunked prefill: 4 sequences of 2048/4096/8192/8192 tokens from empty prefixes, H=32, "
+                        "dk=dv=128, chunk 64, checkpoints every 128 tokens (176 x 32 heads) into pool slots",
+            "tokens_per_s": T * ws / (ms / 1000.0), "ms_per_call": ms, "steps": Kp,
+            "status": int(status.item()),
+            "hbm_frac_of_algorithmic_bytes": io / (ms / 1000.0) / 1e9 / hbm_peak,
+            "algorithmic_bytes_per_call": io}
+
+
+def run_profile_case(args):
+    """Small case for ncu captures of one kernel: decode on a 768-slot pool (1.5 GiB, larger than L2),
+    batch 64, a fresh slot draw per launch; or one prefill call of the benchmark's prefill workload."""
+    import torch
+    import hybrid_linear_attention_decode_gb300 as kda
+    kda.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    seed = 2
+    wts = ki.layer_weights(seed, H, DK, DV, W)
+    prm = kda.LayerParams(torch.from_numpy(wts["conv_w"]).to(dev), torch.from_numpy(wts["norm_w"]).to(dev))
+    if args.profile == "decode":
+        slots_n = 768
+        pool = kda.StatePool.empty(slots_n, H, DK, DV, W, device=dev)
+        ki.fill_device_pool(pool.S, pool.conv, seed)
+        tok = ki.token_inputs(seed, DEC_N, H, DK, DV)
+        d = {k: bf16_dev(v, dev) for k, v in tok.items()}
+        y = torch.empty(DEC_N, H, DV, dtype=torch.bfloat16, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        n = args.warmup + args.steps
+        slots = torch.rand(n, slots_n, device=dev, generator=g).argsort(dim=1)[:, :DEC_N].to(torch.int32).contiguous()
+        for i in range(n):
+            kda.kda_decode_step(pool, prm, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y, slots[i], slots[i],
+                                status, stream)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        print(f"profile case decode: {n} launches")
+    else:
+        pool = kda.StatePool.empty(512, H, DK, DV, W, device=dev)
+        r = run_prefill(argparse.Namespace(steps=1, warmup=args.warmup), kda, torch, dev, stream, pool, prm, seed,
+                        6666.0, 1)
+        print(f"profile case prefill: {r}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+                    help="run a small case of one kernel for an ncu capture and exit")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

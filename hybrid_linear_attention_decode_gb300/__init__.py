@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 _lib = None
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED_SHAPE, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = 0, 1, 2, 3, 4
-KDA_DEV_BAD_SLOT, KDA_DEV_BAD_SEQLENS, KDA_DEV_BAD_CKPT, KDA_DEV_DECAY_RANGE, KDA_DEV_TIMEOUT = 1, 2, 4, 8, 16
+KDA_DEV_BAD_SLOT, KDA_DEV_BAD_SEQLENS, KDA_DEV_BAD_CKPT, KDA_DEV_TIMEOUT = 1, 2, 4, 16
 
 
 class KdaError(RuntimeError):

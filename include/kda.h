@@ -22,8 +22,7 @@
  * 16-byte aligned.  bf16 tensors are passed as their uint16 bit patterns.
  *
  * Errors: problems visible on the host return a kda_status before anything is launched.  Problems only
- * visible on the device (an out-of-range slot index, inconsistent sequence or checkpoint tables, a
- * decay logit outside the chunked form's range) OR a bit into *dev_status (a device int32 the caller
+ * visible on the device (an out-of-range slot index, inconsistent sequence or checkpoint tables) OR a bit into *dev_status (a device int32 the caller
  * zeroes and reads after synchronising) and skip the affected work item; kernels never trap.
  */
 #ifndef KDA_H
@@ -58,15 +57,7 @@ enum kda_status {
 #define KDA_DEV_BAD_SLOT 0x1      /* a slot index outside [0, num_slots) (src may also be -1) */
 #define KDA_DEV_BAD_SEQLENS 0x2   /* cu_seqlens not non-decreasing from 0 to total_tokens, or start_pos < 0 */
 #define KDA_DEV_BAD_CKPT 0x4      /* ckpt_offsets does not give sequence n exactly its boundary count */
-#define KDA_DEV_DECAY_RANGE 0x8   /* prefill: a decay logit below -KDA_MIN_DECAY_LOGIT's range (see below) */
 #define KDA_DEV_TIMEOUT 0x10      /* a bounded wait on an asynchronous copy gave up */
-
-/*
- * Chunked prefill evaluates exp(+-cumulative log-decay) over half a 16-token sub-block; to stay inside
- * fp32 range each per-token decay logit must satisfy a >= KDA_MIN_DECAY_LOGIT (alpha >= ~4.5e-5).
- * Tokens below it set KDA_DEV_DECAY_RANGE.  Decode has no such limit.
- */
-#define KDA_MIN_DECAY_LOGIT (-10.0f)
 
 /*
  * The state-slot pool ("The Hardest Part: Prefix Caching for KDA": the physical state block is

@@ -129,3 +129,30 @@ def pool_tiles(seed: int, H: int, dk: int, dv: int, W: int, units: np.ndarray, s
 def random_slots(seed: int, num_slots: int, n: int, draw: int = 0) -> np.ndarray:
     """n distinct slots out of num_slots (draw selects an independent draw)."""
     return permutation(seed, STREAM["slots"] + 1000 * draw, num_slots)[:n].astype(np.int32)
+
+
+def fill_device_pool(pool_S, pool_conv, seed: int, unique: int = 256):
+    """Fill a device pool (torch tensors S [slots,H,dk,dv] fp32, conv [slots,H,W-1,Cc] bf16) so that
+    (slot, head) unit u holds the contents of generated unit u % unique.  Returns the host copies of
+    the unique units (S [U,dk,dv] fp32, conv [U,W-1,Cc] uint16)."""
+    import torch
+    ns, H, dk, dv = pool_S.shape
+    W = pool_conv.shape[2] + 1
+    U = min(unique, ns * H)
+    S_h, C_h = pool_tiles(seed, H, dk, dv, W, np.arange(U))
+    S_d = torch.from_numpy(S_h).to(pool_S.device)
+    C_d = torch.from_numpy(C_h.view(np.int16)).to(pool_S.device).view(torch.bfloat16)
+    flatS = pool_S.view(ns * H, dk, dv)
+    flatC = pool_conv.view(ns * H, W - 1, 2 * dk + dv)
+    for start in range(0, ns * H, U):
+        m = min(U, ns * H - start)
+        flatS[start:start + m].copy_(S_d[:m])
+        flatC[start:start + m].copy_(C_d[:m])
+    return S_h, C_h
+
+
+def pool_unit_values(S_h, C_h, slot: int, H: int):
+    """Values held by slot `slot` (all heads) of a pool filled by fill_device_pool: S fp64, conv fp64."""
+    U = S_h.shape[0]
+    idx = [(slot * H + h) % U for h in range(H)]
+    return S_h[idx].astype(np.float64), bf16_bits_to_f64(C_h[idx])

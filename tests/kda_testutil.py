@@ -40,26 +40,8 @@ def s_err(S, ref) -> float:
 
 
 def fill_pool(pool, seed: int, unique: int = 256):
-    """Fill every (slot, head) unit of a device pool from `unique` host-generated units, unit u
-    holding the contents of unit u % unique.  Returns the host copies (S [unique,dk,dv] fp32,
-    conv [unique,W-1,Cc] uint16)."""
-    ns, H, dk, dv = pool.S.shape
-    W = pool.conv.shape[2] + 1
-    U = min(unique, ns * H)
-    S_h, C_h = ki.pool_tiles(seed, H, dk, dv, W, np.arange(U))
-    S_d = torch.from_numpy(S_h).cuda()
-    C_d = to_dev_bf16(C_h)
-    flatS = pool.S.view(ns * H, dk, dv)
-    flatC = pool.conv.view(ns * H, W - 1, 2 * dk + dv)
-    for start in range(0, ns * H, U):
-        m = min(U, ns * H - start)
-        flatS[start:start + m].copy_(S_d[:m])
-        flatC[start:start + m].copy_(C_d[:m])
-    return S_h, C_h
+    return ki.fill_device_pool(pool.S, pool.conv, seed, unique)
 
 
 def pool_unit_host(S_h, C_h, slot: int, H: int):
-    """Host contents of slot `slot` (all heads) for a pool filled by fill_pool."""
-    U = S_h.shape[0]
-    idx = [(slot * H + h) % U for h in range(H)]
-    return S_h[idx].astype(np.float64), ki.bf16_bits_to_f64(C_h[idx])
+    return ki.pool_unit_values(S_h, C_h, slot, H)

@@ -1,0 +1,271 @@
+"""Chunked prefill with checkpoint emission on the GPU (through the C ABI) against the fp64 oracle.
+
+Bars: bf16 outputs within 2e-2 (max over (token, head) of max|y - y_ref| / max|y_ref|); fp32 states
+(final and every checkpoint) within 1e-3 relative Frobenius per (sequence, head); conv windows, slot
+placement and every untouched slot bit-exact; resume == replay bit-exact GPU against GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as ki
+import oracle
+from tests.kda_testutil import (S_TOL, Y_TOL, bf16_dev_bits, bf16_dev_to_f64, fill_pool, pool_unit_host, s_err,
+                                to_dev_bf16, y_err)
+
+pytestmark = pytest.mark.gpu
+
+
+def _kda():
+    import hybrid_linear_attention_decode_gb300 as kda
+    kda.load_library()
+    return kda
+
+
+class Problem:
+    """A varlen prefill call: sequences, start positions, slots, checkpoint table, inputs."""
+
+    def __init__(self, kda, H, dk, dv, lens, starts, src, dst, chunk, interval, num_slots, seed, with_z=True,
+                 fill=True, ckpt_skip=()):
+        self.kda, self.H, self.dk, self.dv = kda, H, dk, dv
+        self.lens, self.starts, self.src, self.dst = list(lens), list(starts), list(src), list(dst)
+        self.chunk, self.interval, self.num_slots = chunk, interval, num_slots
+        self.T = int(sum(lens))
+        self.cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        self.pool = kda.StatePool.empty(num_slots, H, dk, dv)
+        self.S_h, self.C_h = fill_pool(self.pool, seed) if fill else (None, None)
+        self.wts = ki.layer_weights(seed, H, dk, dv)
+        self.prm = kda.LayerParams(torch.from_numpy(self.wts["conv_w"]).cuda(),
+                                   torch.from_numpy(self.wts["norm_w"]).cuda())
+        self.tok = ki.token_inputs(seed, self.T, H, dk, dv, with_z=with_z)
+        counts = [oracle.ckpt_count(s, l, interval) if interval else 0 for s, l in zip(starts, lens)]
+        self.offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        used = set(x for x in src if x >= 0) | set(dst)
+        free = [s for s in range(num_slots) if s not in used]
+        nck = int(self.offs[-1])
+        assert len(free) >= nck
+        self.ck = np.array(free[:nck], dtype=np.int32)
+        for j in ckpt_skip:
+            self.ck[j] = -1
+
+    def run(self, status=None):
+        kda = self.kda
+        d = {k: (to_dev_bf16(v) if v is not None else None) for k, v in self.tok.items()}
+        self.y = torch.empty(self.T, self.H, self.dv, dtype=torch.bfloat16, device="cuda")
+        nbytes = kda.kda_prefill_workspace_bytes(self.pool, len(self.lens), self.T, self.chunk)
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+        ws.fill_(0xAB)  # contents need not be initialised
+        self.status = status if status is not None else torch.zeros(1, dtype=torch.int32, device="cuda")
+        t = lambda a, dt: torch.tensor(np.asarray(a), dtype=dt, device="cuda")  # noqa: E731
+        kda.kda_prefill_chunked(self.pool, self.prm, t(self.cu, torch.int32), t(self.starts, torch.int64),
+                                t(self.src, torch.int32), t(self.dst, torch.int32), self.chunk, self.interval,
+                                t(self.offs, torch.int32), t(self.ck if len(self.ck) else [0], torch.int32),
+                                d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], self.y, ws, self.status)
+        torch.cuda.synchronize()
+        return int(self.status.item())
+
+    def reference(self, heads=None):
+        """fp64 oracle over all sequences for the given heads (all by default)."""
+        heads = list(range(self.H)) if heads is None else list(heads)
+        Hs, dk, dv = len(heads), self.dk, self.dv
+        cfg = oracle.Cfg(H=Hs, dk=dk, dv=dv)
+        N = len(self.lens)
+        S0 = np.zeros((N, Hs, dk, dv))
+        C0 = np.zeros((N, Hs, 3, 2 * dk + dv))
+        for n, s in enumerate(self.src):
+            if s >= 0:
+                Sa, Ca = pool_unit_host(self.S_h, self.C_h, s, self.H)
+                S0[n], C0[n] = Sa[heads], Ca[heads]
+        f = {k: (ki.bf16_bits_to_f64(v)[:, heads] if v is not None else None) for k, v in self.tok.items()}
+        return oracle.forward(cfg, self.cu, np.array(self.starts, dtype=np.int64), f["q"], f["k"], f["v"], f["a"],
+                              f["b"], f["z"], self.wts["conv_w"][heads], self.wts["norm_w"], S0, C0,
+                              interval=self.interval)
+
+    def check(self, ref, heads=None):
+        heads = list(range(self.H)) if heads is None else list(heads)
+        yg = bf16_dev_to_f64(self.y)[:, heads]
+        assert y_err(yg, ref["y"]) <= Y_TOL
+        for n, d in enumerate(self.dst):
+            Sg = self.pool.S[d].cpu().numpy()[heads]
+            assert s_err(Sg, ref["S"][n]) <= S_TOL, ("final", n)
+            np.testing.assert_array_equal(ki.bf16_bits_to_f64(bf16_dev_bits(self.pool.conv[d]))[heads],
+                                          ref["conv"][n])
+        for j, slot in enumerate(self.ck):
+            if slot < 0:
+                continue
+            Sg = self.pool.S[int(slot)].cpu().numpy()[heads]
+            assert s_err(Sg, ref["ckpt_S"][j]) <= S_TOL, ("ckpt", j, int(ref["ckpt_pos"][j]))
+            np.testing.assert_array_equal(ki.bf16_bits_to_f64(bf16_dev_bits(self.pool.conv[int(slot)]))[heads],
+                                          ref["ckpt_conv"][j])
+
+
+SHAPES = [(16, 16), (32, 16), (16, 32), (64, 64), (128, 128)]
+
+
+@pytest.mark.parametrize("dk,dv", SHAPES)
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_prefill_matches_oracle_varlen(dk, dv, chunk):
+    """Ragged sequences, non-zero start positions (resumed states), fresh and moved slots, checkpoints
+    (one skipped), a zero-length sequence; every slot that is neither a destination nor a checkpoint
+    is bit-for-bit unchanged."""
+    kda = _kda()
+    interval = 2 * chunk
+    lens = [3 * chunk + 5, 1, chunk - 3, 0, 2 * chunk]
+    starts = [0, 7, 2 * chunk + 1, 5, interval]
+    src = [-1, 3, 4, 6, 9]
+    dst = [2, 3, 5, 7, 10]
+    p = Problem(kda, 3, dk, dv, lens, starts, src, dst, chunk, interval, 40, seed=dk * 7 + dv + chunk,
+                ckpt_skip=(1,))
+    before_S, before_C = p.pool.S.clone(), p.pool.conv.clone()
+    assert p.run() == 0
+    p.check(p.reference())
+    written = set(dst) | set(int(x) for x in p.ck if x >= 0)
+    keep = [s for s in range(40) if s not in written]
+    assert torch.equal(p.pool.S[keep], before_S[keep])
+    assert torch.equal(p.pool.conv[keep].view(torch.int16), before_C[keep].view(torch.int16))
+
+
+def test_prefill_no_gate_and_no_checkpoints():
+    kda = _kda()
+    p = Problem(kda, 2, 128, 128, [100, 37], [0, 64], [-1, 1], [0, 1], 64, 0, 8, seed=5, with_z=False)
+    assert p.run() == 0
+    p.check(p.reference())
+
+
+def test_tiny_configuration_end_to_end():
+    """The tiny configuration: H=2, dk=dv=16, a 64-token prefill from an empty prefix (chunk 16,
+    checkpoints every 32 tokens), 8 decode steps from the final state, and a resume from the checkpoint
+    at 32 replayed to 64 -- all against the oracle; resume vs replay bit-exact on the GPU."""
+    kda = _kda()
+    H, D, T = 2, 16, 64
+    p = Problem(kda, H, D, D, [T], [0], [-1], [0], 16, 32, 8, seed=1)
+    assert p.run() == 0
+    ref = p.reference()
+    p.check(ref)
+    assert list(ref["ckpt_pos"]) == [32, 64]
+    ck32, ck64 = int(p.ck[0]), int(p.ck[1])
+    # 8 decode steps from slot 0
+    tok = ki.token_inputs(11, 8, H, D, D)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ys = []
+    for s in range(8):
+        d = {k: to_dev_bf16(np.ascontiguousarray(v[s:s + 1])) for k, v in tok.items()}
+        y = torch.empty(1, H, D, dtype=torch.bfloat16, device="cuda")
+        sl = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kda.kda_decode_step(p.pool, p.prm, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y, sl, sl, status)
+        ys.append(bf16_dev_to_f64(y)[0])
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    f = {k: ki.bf16_bits_to_f64(v) for k, v in tok.items()}
+    cfg = oracle.Cfg(H=H, dk=D, dv=D)
+    dec = oracle.forward(cfg, [0, 8], [T], f["q"], f["k"], f["v"], f["a"], f["b"], f["z"], p.wts["conv_w"],
+                         p.wts["norm_w"], ref["S"], ref["conv"])
+    assert y_err(np.array(ys), dec["y"]) <= Y_TOL
+    assert s_err(p.pool.S[0].cpu().numpy(), dec["S"][0]) <= S_TOL
+    # resume from the checkpoint at 32 into a private slot, replay tokens 32..63
+    kda.kda_resume_from_slot(p.pool, torch.tensor([ck32], dtype=torch.int32, device="cuda"),
+                             torch.tensor([5], dtype=torch.int32, device="cuda"), status)
+    q = Problem.__new__(Problem)
+    q.__dict__.update(p.__dict__)
+    q.lens, q.starts, q.src, q.dst, q.T = [32], [32], [5], [5], 32
+    q.cu = np.array([0, 32], dtype=np.int32)
+    q.tok = {k: np.ascontiguousarray(v[32:]) for k, v in p.tok.items()}
+    q.offs = np.array([0, 1], dtype=np.int32)
+    q.ck = np.array([6], dtype=np.int32)
+    y_full = p.y.clone()
+    assert q.run() == 0
+    assert torch.equal(q.y.view(torch.int16), y_full[32:].view(torch.int16))
+    assert torch.equal(p.pool.S[6], p.pool.S[ck64]) and torch.equal(p.pool.S[5], p.pool.S[ck64])
+    assert torch.equal(p.pool.conv[5].view(torch.int16), p.pool.conv[ck64].view(torch.int16))
+
+
+def test_resume_equals_replay_bitwise_shared_prefix():
+    """Several requests share one prefix: each resumes from the prefix's last checkpoint (copy-on-write
+    into a private slot) and prefills its own suffix; each result equals, bit for bit, a full replay of
+    prefix + suffix, and the shared checkpoint slot is left untouched."""
+    kda = _kda()
+    H, D, C, I, P, R, L = 4, 128, 64, 128, 1024 + 40, 3, 200
+    b = (P // I) * I  # largest checkpoint boundary inside the shared prefix
+    base = ki.token_inputs(41, P, H, D, D)
+    full = Problem(kda, H, D, D, [P], [0], [-1], [0], C, I, 64, seed=41)
+    full.tok = base
+    assert full.run() == 0
+    j = list(oracle.ckpt_positions(0, P, I)).index(b)
+    shared = int(full.ck[j])
+    shared_before = (full.pool.S[shared].clone(), full.pool.conv[shared].clone())
+    suffixes = [ki.token_inputs(100 + r, L, H, D, D) for r in range(R)]
+    # resumed: copy-on-write into private slots 50.., then one varlen call for all suffixes (tokens b.. P+L)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    priv = list(range(50, 50 + R))
+    kda.kda_resume_from_slot(full.pool, torch.tensor([shared] * R, dtype=torch.int32, device="cuda"),
+                             torch.tensor(priv, dtype=torch.int32, device="cuda"), status)
+    res = Problem.__new__(Problem)
+    res.__dict__.update(full.__dict__)
+    seg = [{k: np.concatenate([base[k][b:], suffixes[r][k]]) for k in base} for r in range(R)]
+    res.lens, res.starts, res.src, res.dst = [P - b + L] * R, [b] * R, priv, priv
+    res.T = R * (P - b + L)
+    res.cu = np.arange(R + 1, dtype=np.int32) * (P - b + L)
+    res.tok = {k: np.concatenate([s[k] for s in seg]) for k in base}
+    res.offs = np.zeros(R + 1, dtype=np.int32)
+    res.ck = np.zeros(0, dtype=np.int32)
+    res.interval = 0
+    assert res.run() == 0
+    y_res = res.y.clone()
+    assert torch.equal(full.pool.S[shared], shared_before[0])
+    assert torch.equal(full.pool.conv[shared].view(torch.int16), shared_before[1].view(torch.int16))
+    # full replays of prefix + suffix, one call each
+    for r in range(R):
+        rep = Problem.__new__(Problem)
+        rep.__dict__.update(full.__dict__)
+        rep.lens, rep.starts, rep.src, rep.dst = [P + L], [0], [-1], [60 + r]
+        rep.T = P + L
+        rep.cu = np.array([0, P + L], dtype=np.int32)
+        rep.tok = {k: np.concatenate([base[k], suffixes[r][k]]) for k in base}
+        rep.offs = np.zeros(2, dtype=np.int32)
+        rep.ck = np.zeros(0, dtype=np.int32)
+        rep.interval = 0
+        assert rep.run() == 0
+        seg_len = P - b + L
+        assert torch.equal(rep.y[b:].view(torch.int16), y_res[r * seg_len:(r + 1) * seg_len].view(torch.int16))
+        assert torch.equal(full.pool.S[60 + r], full.pool.S[priv[r]])
+        assert torch.equal(full.pool.conv[60 + r].view(torch.int16), full.pool.conv[priv[r]].view(torch.int16))
+    # and the resumed results match the oracle
+    f_ref = rep.reference(heads=[0, 3])  # the last replay, oracle
+    yg = bf16_dev_to_f64(y_res[(R - 1) * (P - b + L):])[:, [0, 3]]
+    assert y_err(yg, f_ref["y"][b:]) <= Y_TOL
+
+
+def test_prefill_bad_tables_flag_status():
+    kda = _kda()
+    # checkpoint offsets that do not match the boundary count: flagged, no checkpoint written
+    p = Problem(kda, 2, 16, 16, [40, 20], [0, 0], [-1, -1], [0, 1], 16, 16, 16, seed=3)
+    p.offs = np.array([0, 1, 2], dtype=np.int32)  # should be [0, 2, 3]: sequence 0 is inconsistent
+    before = p.pool.S.clone()
+    st = p.run()
+    assert st & kda.KDA_DEV_BAD_CKPT
+    untouched = [s for s in range(16) if s not in (0, 1, int(p.ck[1]))]  # seq 1's entry is consistent
+    assert torch.equal(p.pool.S[untouched], before[untouched])
+    # a destination slot out of range: that sequence is skipped, the other one is computed
+    p2 = Problem(kda, 2, 16, 16, [40, 20], [0, 0], [-1, -1], [0, 99], 16, 0, 16, seed=3)
+    st = p2.run()
+    assert st & kda.KDA_DEV_BAD_SLOT
+    ref = p2.reference()
+    assert y_err(bf16_dev_to_f64(p2.y)[:40], ref["y"][:40]) <= Y_TOL
+    # cu_seqlens not ending at total_tokens
+    p3 = Problem(kda, 2, 16, 16, [40, 20], [0, 0], [-1, -1], [0, 1], 16, 0, 16, seed=3)
+    p3.cu = np.array([0, 40, 50], dtype=np.int32)
+    assert p3.run() & kda.KDA_DEV_BAD_SEQLENS
+
+
+def test_prefill_full_size_sampled_heads():
+    """The chunked-prefill workload at full size (4 sequences of 2048/4096/8192/8192 tokens, H=32,
+    dk=dv=128, chunk 64, checkpoints every 128 tokens: 176 boundaries), in the launch configuration the
+    benchmark times; two heads against the oracle at every output, every checkpoint and the final states."""
+    kda = _kda()
+    lens = [2048, 4096, 8192, 8192]
+    p = Problem(kda, 32, 128, 128, lens, [0] * 4, [-1] * 4, [0, 1, 2, 3], 64, 128, 256, seed=3, fill=False)
+    assert p.run() == 0
+    assert len(p.ck) == 176
+    heads = [0, 21]
+    ref = p.reference(heads)
+    p.check(ref, heads)
