@@ -7,12 +7,13 @@
 //
 // The step is a stream over fp32 states (64 KiB per request and head at dk = dv = 128): each state is
 // read once and written once.  Design:
-//   * persistent CTAs (one per SM at dk = dv = 128), each walking work items (request, head) with a
+//   * persistent CTAs (two per SM at dk = dv = 128), each walking work items (request, head) with a
 //     stride of gridDim.x, heads fastest so that neighbouring CTAs stream neighbouring 64 KiB tiles of
 //     one slot;
 //   * every input of an item -- the state in NST stages, the raw conv window, q, k, v, a, z -- arrives
-//     by 1-D bulk TMA copies into one of NBUF shared-memory buffers, completion counted on mbarriers,
-//     so that the next items' bytes are in flight while the current item computes;
+//     by 1-D bulk TMA copies into one of NBUF shared-memory buffers, completion counted on mbarriers;
+//     the state moves to registers in the first pass, after which the buffer is handed to the copies
+//     of a later item, so loads overlap the rest of the item and the other CTA's work;
 //   * one pass over S' = Diag(alpha) S reduces k^T S' and q^T S' together (o = S'^T q + beta (k.q) u
 //     with u = v - S'^T k), a second pass writes S' + beta k u^T with 128-bit coalesced stores;
 //   * conv, norms and gates use warp reductions in a fixed order, so the kernel is deterministic.
@@ -31,6 +32,7 @@ struct DecodeShape {
     static constexpr int RPT = DK / RPP;      // rows per thread
     static constexpr int NST = (DK >= 128) ? 4 : 1;
     static constexpr int M_ST = RPT / NST;    // rows per thread per stage
+    static constexpr int CPT = (CC + NT - 1) / NT;  // conv channels per thread
     static constexpr uint32_t S_BYTES = DK * DV * 4;
     static constexpr uint32_t ST_BYTES = S_BYTES / NST;
     static constexpr uint32_t CONV_BYTES = (W - 1) * CC * 2;
@@ -41,23 +43,24 @@ struct DecodeShape {
     static constexpr uint32_t OFF_A = OFF_V + DV * 2;
     static constexpr uint32_t OFF_Z = OFF_A + DK * 2;
     static constexpr uint32_t BUF_BYTES = (OFF_Z + DV * 2 + 127) / 128 * 128;
-    static constexpr int NF = 2 * RPP * DV + CC + 4 * DK + 2 * DV + 16;  // float scratch
+    static constexpr int NF = 2 * RPP * DV + CC + 4 * DK + 3 * DV;  // float scratch
     static constexpr uint32_t OFF_F = NBUF * BUF_BYTES;
     static constexpr uint32_t OFF_BAR = (OFF_F + NF * 4 + 15) / 16 * 16;
     static constexpr uint32_t SMEM = OFF_BAR + NBUF * (1 + NST) * 8;
+    static constexpr int MIN_BLOCKS = (NBUF == 1 && DK * DV >= 4096) ? 2 : 1;
 
-    static_assert(DV % 4 == 0 && 32 % LPR == 0 || LPR == 32, "row mapping");
+    static_assert(LPR <= 32 && 32 % LPR == 0, "row mapping");
+    static_assert(DV <= NT, "one output channel per thread in the epilogue");
     static_assert(RPP * RPT == DK && RPT % NST == 0, "row split");
     static_assert(CONV_BYTES % 16 == 0 && (DK * 2) % 16 == 0 && (DV * 2) % 16 == 0, "bulk copy sizes");
     static_assert(OFF_CONV % 16 == 0 && OFF_Q % 16 == 0 && OFF_V % 16 == 0 && OFF_A % 16 == 0, "align");
-    static_assert(NT >= 64, "two warps needed for the norm reductions");
 };
 
 template <int DK, int DV, int NBUF>
-__global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT)
+__global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT, DecodeShape<DK, DV, NBUF>::MIN_BLOCKS)
     kda_decode_kernel(const DecodeArgs args) {
     using C = DecodeShape<DK, DV, NBUF>;
-    constexpr int NT = C::NT, CC = C::CC, NST = C::NST, RPP = C::RPP, LPR = C::LPR;
+    constexpr int NT = C::NT, CC = C::CC, NST = C::NST, RPP = C::RPP, LPR = C::LPR, RPT = C::RPT;
     extern __shared__ __align__(128) uint8_t smem[];
     float *red_k = reinterpret_cast<float *>(smem + C::OFF_F);  // [RPP][DV]
     float *red_q = red_k + RPP * DV;                              // [RPP][DV]
@@ -68,11 +71,11 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT)
     float *al = qa + DK;                                          // [DK] alpha
     float *bu = al + DK;                                          // [DV] beta * u
     float *os = bu + DV;                                          // [DV] o
-    float *scal = os + DV;                                        // [16]
+    float *nw = os + DV;                                          // [DV] RMSNorm weight
     uint64_t *bar_in = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);  // [NBUF]
     uint64_t *bar_S = bar_in + NBUF;                                      // [NBUF][NST]
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int H = args.H;
     const int nitems = args.n * H;
     const int64_t ns = args.num_slots;
@@ -81,6 +84,7 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT)
         for (int i = 0; i < NBUF * (1 + NST); ++i) mbar_init(&bar_in[i], 1);
         fence_mbar_init();
     }
+    for (int j = tid; j < DV; j += NT) nw[j] = __ldg(args.norm_w + j);
     __syncthreads();
 
     // Thread 0: start every copy of `item` into buffer `buf`.  Each barrier of the buffer is arrived
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT)
         const int buf = it % NBUF;
         const uint32_t par = (uint32_t)(it / NBUF) & 1u;
         const int n = item / H, h = item - (item / H) * H;
-        const int src = args.src[n], dst = args.dst[n];
+        const int src = __ldg(args.src + n), dst = __ldg(args.dst + n);
         const bool ok = src >= -1 && src < ns && dst >= 0 && dst < ns;
         const size_t th = (size_t)n * H + h;
         uint8_t *bp = smem + (size_t)buf * C::BUF_BYTES;
@@ -140,6 +144,15 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT)
         const uint16_t *a_s = reinterpret_cast<const uint16_t *>(bp + C::OFF_A);
         const uint16_t *z_s = reinterpret_cast<const uint16_t *>(bp + C::OFF_Z);
 
+        // global loads that do not depend on the copies: issued before the wait
+        float4 wc[C::CPT];
+#pragma unroll
+        for (int u = 0; u < C::CPT; ++u) {
+            const int c = tid + u * NT;
+            if (c < CC) wc[u] = __ldg(reinterpret_cast<const float4 *>(args.conv_w + ((size_t)h * CC + c) * 4));
+        }
+        const float beta = ok ? sigmoidf_(bf2f(__ldg(args.b + th))) : 0.f;
+
         bool fail = !mbar_wait(&bar_in[buf], par);
         if (__syncthreads_or(fail)) {
             if (tid == 0) set_status(args.status, KDA_DEV_TIMEOUT);
@@ -148,120 +161,121 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT)
         if (!ok) {
             for (int j = tid; j < DV; j += NT) args.y[th * DV + j] = 0;
             if (tid == 0) set_status(args.status, KDA_DEV_BAD_SLOT);
-        } else {
-            // ---- causal conv (+ SiLU) over the q | k | v channels; the new raw window goes to dst ----
-            uint16_t *cd = args.conv + ((size_t)dst * H + h) * (C::W - 1) * CC;
-            for (int c = tid; c < CC; c += NT) {
-                const uint16_t xr = q_s[c];  // q, k, v are contiguous in the buffer
-                uint16_t w0 = 0, w1 = 0, w2 = 0;
-                if (src >= 0) {
-                    w0 = cs[c];
-                    w1 = cs[CC + c];
-                    w2 = cs[2 * CC + c];
-                }
-                const float4 w = __ldg(reinterpret_cast<const float4 *>(args.conv_w + ((size_t)h * CC + c) * 4));
-                float acc = w.w * bf2f(xr);
-                acc = fmaf(w.x, bf2f(w0), acc);
-                acc = fmaf(w.y, bf2f(w1), acc);
-                acc = fmaf(w.z, bf2f(w2), acc);
-                if (args.silu) acc = acc / (1.0f + __expf(-acc));
-                xs[c] = acc;
-                cd[c] = w1;
-                cd[CC + c] = w2;
-                cd[2 * CC + c] = xr;
+            __syncthreads();  // every read of this buffer is done
+            if (tid == 0) {
+                fence_proxy_async_smem();
+                issue(buf, item + NBUF * gridDim.x);
             }
-            __syncthreads();
-            if (warp == 0) {
-                const float nq = warp_dot_array(xs, xs, DK);
-                const float qk = warp_dot_array(xs, xs + DK, DK);
-                if (lane == 0) { scal[0] = nq; scal[2] = qk; }
-            } else if (warp == 1) {
-                const float nk = warp_dot_array(xs + DK, xs + DK, DK);
-                if (lane == 0) scal[1] = nk;
-            }
-            __syncthreads();
-            const float rq = rsqrtf(scal[0] + args.l2_eps), rk = rsqrtf(scal[1] + args.l2_eps);
-            const float kq = scal[2] * rq * rk;
-            const float beta = sigmoidf_(bf2f(args.b[th]));
-            for (int i = tid; i < DK; i += NT) {
-                const float alpha = sigmoidf_(bf2f(a_s[i]));
-                const float k_ = xs[DK + i] * rk;
-                kh[i] = k_;
-                al[i] = alpha;
-                ka[i] = alpha * k_;
-                qa[i] = alpha * (xs[i] * rq);
-            }
-            __syncthreads();
-
-            // ---- pass 1: column sums of k^T S' and q^T S' ----
-            float4 accK = make_float4(0.f, 0.f, 0.f, 0.f), accQ = accK;
-            bool sfail = false;
-            if (src >= 0) {
-#pragma unroll
-                for (int s = 0; s < NST; ++s) {
-                    sfail |= !mbar_wait(&bar_S[buf * NST + s], par);
-#pragma unroll
-                    for (int m = 0; m < C::M_ST; ++m) {
-                        const int row = g + (s * C::M_ST + m) * RPP;
-                        const float4 x = *reinterpret_cast<const float4 *>(Ss + row * DV + cg * 4);
-                        const float kk = ka[row], qq = qa[row];
-                        accK.x = fmaf(kk, x.x, accK.x); accK.y = fmaf(kk, x.y, accK.y);
-                        accK.z = fmaf(kk, x.z, accK.z); accK.w = fmaf(kk, x.w, accK.w);
-                        accQ.x = fmaf(qq, x.x, accQ.x); accQ.y = fmaf(qq, x.y, accQ.y);
-                        accQ.z = fmaf(qq, x.z, accQ.z); accQ.w = fmaf(qq, x.w, accQ.w);
-                    }
-                }
-            }
-            *reinterpret_cast<float4 *>(red_k + g * DV + cg * 4) = accK;
-            *reinterpret_cast<float4 *>(red_q + g * DV + cg * 4) = accQ;
-            if (__syncthreads_or(sfail)) {
-                if (tid == 0) set_status(args.status, KDA_DEV_TIMEOUT);
-                return;
-            }
-            for (int j = tid; j < DV; j += NT) {
-                float kS = 0.f, qS = 0.f;
-#pragma unroll
-                for (int r = 0; r < RPP; ++r) {
-                    kS += red_k[r * DV + j];
-                    qS += red_q[r * DV + j];
-                }
-                const float u = xs[2 * DK + j] - kS;
-                os[j] = args.scale * fmaf(beta * kq, u, qS);
-                bu[j] = beta * u;
-            }
-            __syncthreads();
-            if (warp == 0) {
-                const float ss = warp_dot_array(os, os, DV);
-                if (lane == 0) scal[3] = rsqrtf(ss * (1.0f / DV) + args.rms_eps);
-            }
-            __syncthreads();
-            const float rr = scal[3];
-            for (int j = tid; j < DV; j += NT) {
-                float yv = os[j] * rr * __ldg(args.norm_w + j);
-                if (args.z) yv *= sigmoidf_(bf2f(z_s[j]));
-                args.y[th * DV + j] = f2bf(yv);
-            }
-            // ---- pass 2: S_new = Diag(alpha) S + k^ (beta u)^T, 128-bit stores ----
-            float *Sd = args.S + ((size_t)dst * H + h) * DK * DV;
-            const float4 b4 = *reinterpret_cast<const float4 *>(bu + cg * 4);
-#pragma unroll 4
-            for (int m = 0; m < C::RPT; ++m) {
-                const int row = g + m * RPP;
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (src >= 0) x = *reinterpret_cast<const float4 *>(Ss + row * DV + cg * 4);
-                const float aa = al[row], kk = kh[row];
-                float4 o4;
-                o4.x = fmaf(kk, b4.x, aa * x.x);
-                o4.y = fmaf(kk, b4.y, aa * x.y);
-                o4.z = fmaf(kk, b4.z, aa * x.z);
-                o4.w = fmaf(kk, b4.w, aa * x.w);
-                *reinterpret_cast<float4 *>(Sd + row * DV + cg * 4) = o4;
-            }
+            continue;
         }
-        __syncthreads();  // every read of this buffer is done
+        // ---- causal conv (+ SiLU) over the q | k | v channels; the new raw window goes to dst ----
+        uint16_t *cd = args.conv + ((size_t)dst * H + h) * (C::W - 1) * CC;
+#pragma unroll
+        for (int u = 0; u < C::CPT; ++u) {
+            const int c = tid + u * NT;
+            if (c >= CC) break;
+            const uint16_t xr = q_s[c];  // q, k, v are contiguous in the buffer
+            uint16_t w0 = 0, w1 = 0, w2 = 0;
+            if (src >= 0) {
+                w0 = cs[c];
+                w1 = cs[CC + c];
+                w2 = cs[2 * CC + c];
+            }
+            const float4 w = wc[u];
+            float acc = w.w * bf2f(xr);
+            acc = fmaf(w.x, bf2f(w0), acc);
+            acc = fmaf(w.y, bf2f(w1), acc);
+            acc = fmaf(w.z, bf2f(w2), acc);
+            if (args.silu) acc = acc / (1.0f + __expf(-acc));
+            xs[c] = acc;
+            cd[c] = w1;
+            cd[CC + c] = w2;
+            cd[2 * CC + c] = xr;
+        }
+        float zg = 1.f;
+        if (args.z && tid < DV) zg = sigmoidf_(bf2f(z_s[tid]));
+        __syncthreads();
+        // every warp reduces |q|^2, |k|^2 and q.k itself (no extra block barrier)
+        const float nq = warp_dot_array(xs, xs, DK);
+        const float nk = warp_dot_array(xs + DK, xs + DK, DK);
+        const float qk = warp_dot_array(xs, xs + DK, DK);
+        const float rq = rsqrtf(nq + args.l2_eps), rk = rsqrtf(nk + args.l2_eps);
+        const float kq = qk * rq * rk;
+        for (int i = tid; i < DK; i += NT) {
+            const float alpha = sigmoidf_(bf2f(a_s[i]));
+            const float k_ = xs[DK + i] * rk;
+            kh[i] = k_;
+            al[i] = alpha;
+            ka[i] = alpha * k_;
+            qa[i] = alpha * (xs[i] * rq);
+        }
+        __syncthreads();
+
+        // ---- pass 1: the state into registers; column sums of k^T S' and q^T S' ----
+        float4 sr[RPT];
+        float4 accK = make_float4(0.f, 0.f, 0.f, 0.f), accQ = accK;
+        bool sfail = false;
+        if (src >= 0) {
+#pragma unroll
+            for (int s = 0; s < NST; ++s) {
+                sfail |= !mbar_wait(&bar_S[buf * NST + s], par);
+#pragma unroll
+                for (int m = 0; m < C::M_ST; ++m) {
+                    const int mm = s * C::M_ST + m;
+                    const int row = g + mm * RPP;
+                    const float4 x = *reinterpret_cast<const float4 *>(Ss + row * DV + cg * 4);
+                    sr[mm] = x;
+                    const float kk = ka[row], qq = qa[row];
+                    accK.x = fmaf(kk, x.x, accK.x); accK.y = fmaf(kk, x.y, accK.y);
+                    accK.z = fmaf(kk, x.z, accK.z); accK.w = fmaf(kk, x.w, accK.w);
+                    accQ.x = fmaf(qq, x.x, accQ.x); accQ.y = fmaf(qq, x.y, accQ.y);
+                    accQ.z = fmaf(qq, x.z, accQ.z); accQ.w = fmaf(qq, x.w, accQ.w);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int mm = 0; mm < RPT; ++mm) sr[mm] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        *reinterpret_cast<float4 *>(red_k + g * DV + cg * 4) = accK;
+        *reinterpret_cast<float4 *>(red_q + g * DV + cg * 4) = accQ;
+        if (__syncthreads_or(sfail)) {
+            if (tid == 0) set_status(args.status, KDA_DEV_TIMEOUT);
+            return;
+        }
+        // the buffer is no longer read: start the copies of a later item into it
         if (tid == 0) {
             fence_proxy_async_smem();
             issue(buf, item + NBUF * gridDim.x);
+        }
+        for (int j = tid; j < DV; j += NT) {
+            float kS = 0.f, qS = 0.f;
+#pragma unroll
+            for (int r = 0; r < RPP; ++r) {
+                kS += red_k[r * DV + j];
+                qS += red_q[r * DV + j];
+            }
+            const float u = xs[2 * DK + j] - kS;
+            os[j] = args.scale * fmaf(beta * kq, u, qS);
+            bu[j] = beta * u;
+        }
+        __syncthreads();
+        const float ss = warp_dot_array(os, os, DV);
+        const float rr = rsqrtf(ss * (1.0f / DV) + args.rms_eps);
+        for (int j = tid; j < DV; j += NT) args.y[th * DV + j] = f2bf(os[j] * rr * nw[j] * zg);
+        // ---- pass 2: S_new = Diag(alpha) S + k^ (beta u)^T from registers, 128-bit stores ----
+        float *Sd = args.S + ((size_t)dst * H + h) * DK * DV;
+        const float4 b4 = *reinterpret_cast<const float4 *>(bu + cg * 4);
+#pragma unroll
+        for (int mm = 0; mm < RPT; ++mm) {
+            const int row = g + mm * RPP;
+            const float aa = al[row], kk = kh[row];
+            const float4 x = sr[mm];
+            float4 o4;
+            o4.x = fmaf(kk, b4.x, aa * x.x);
+            o4.y = fmaf(kk, b4.y, aa * x.y);
+            o4.z = fmaf(kk, b4.z, aa * x.z);
+            o4.w = fmaf(kk, b4.w, aa * x.w);
+            *reinterpret_cast<float4 *>(Sd + row * DV + cg * 4) = o4;
         }
     }
 }
@@ -294,8 +308,13 @@ bool decode_supported(int dk, int dv, int W) {
            (dk == 128 && dv == 128);
 }
 
+// Item buffers per CTA at dk = dv = 128: 1 buffer runs two CTAs per SM, 2 or 3 buffers one CTA per SM.
+#ifndef KDA_DECODE_NBUF_128
+#define KDA_DECODE_NBUF_128 1
+#endif
+
 int launch_decode(const DecodeArgs &a, int dk, int dv, cudaStream_t st) {
-    if (dk == 128 && dv == 128) return launch_decode_t<128, 128, 2>(a, st);
+    if (dk == 128 && dv == 128) return launch_decode_t<128, 128, KDA_DECODE_NBUF_128>(a, st);
     if (dk == 64 && dv == 64) return launch_decode_t<64, 64, 2>(a, st);
     if (dk == 16 && dv == 16) return launch_decode_t<16, 16, 2>(a, st);
     if (dk == 32 && dv == 16) return launch_decode_t<32, 16, 2>(a, st);
