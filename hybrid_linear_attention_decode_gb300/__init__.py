@@ -59,6 +59,9 @@ def load_library(path: str | None = None):
     lib.kda_prefill_chunked.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Params), i32, i64, vp, vp, vp, vp, i32,
                                         i64, vp, vp] + [vp] * 7 + [vp, ctypes.c_size_t, vp, vp]
     lib.kda_prefill_chunked.restype = ctypes.c_int
+    lib.kda_prefill_chunked_noalloc.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Params), i32, i64, vp, vp, vp,
+                                                vp, i32, i64, vp, vp] + [vp] * 7 + [vp, vp]
+    lib.kda_prefill_chunked_noalloc.restype = ctypes.c_int
     lib.kda_resume_from_slot.argtypes = [ctypes.POINTER(_Pool), i32, vp, vp, vp, vp]
     lib.kda_resume_from_slot.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -161,6 +164,26 @@ def kda_prefill_chunked(pool: StatePool, params: LayerParams, cu_seqlens, start_
         _ptr(dst_slot), int(chunk), int(ckpt_interval), _ptr(ckpt_offsets), _ptr(ckpt_slots), _ptr(q), _ptr(k),
         _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(y), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(rc, "kda_prefill_chunked")
+
+
+# Size of the fixed scratch behind kda_prefill_chunked_noalloc (KDA_NOALLOC_SCRATCH_BYTES in kda.h).
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def kda_prefill_chunked_noalloc(pool: StatePool, params: LayerParams, cu_seqlens, start_pos, src_slot, dst_slot,
+                                chunk: int, ckpt_interval: int, ckpt_offsets, ckpt_slots, q, k, v, a, b, z, y,
+                                dev_status, stream=None) -> None:
+    """kda_prefill_chunked for callers that cannot allocate device memory: the workspace is the library's
+    fixed scratch (NOALLOC_SCRATCH_BYTES per GPU).  Calls that overlap on the GPU race on that scratch;
+    the first call on a device should precede any stream capture.  See include/kda.h."""
+    nseq = int(start_pos.shape[0])
+    T = int(q.shape[0]) if q is not None else 0
+    pc, pp = pool.c(), params.c()
+    rc = load_library().kda_prefill_chunked_noalloc(
+        ctypes.byref(pc), ctypes.byref(pp), nseq, T, _ptr(cu_seqlens), _ptr(start_pos), _ptr(src_slot),
+        _ptr(dst_slot), int(chunk), int(ckpt_interval), _ptr(ckpt_offsets), _ptr(ckpt_slots), _ptr(q), _ptr(k),
+        _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(y), _ptr(dev_status), _stream(stream))
+    _check(rc, "kda_prefill_chunked_noalloc")
 
 
 def kda_resume_from_slot(pool: StatePool, src_slot, dst_slot, dev_status, stream=None) -> None:

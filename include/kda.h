@@ -143,6 +143,30 @@ KDA_API int kda_prefill_chunked(const kda_pool *pool, const kda_params *prm, int
                         size_t workspace_bytes, int32_t *dev_status, kda_stream_t stream);
 
 /*
+ * kda_prefill_chunked without a caller-provided workspace (the pages have no counterpart: this is an
+ * interface for callers that cannot allocate device memory -- an engine whose caching allocator owns all
+ * free memory, a plug-in handed only tensors, a process with no device allocation after start-up).
+ * The workspace is a fixed array of KDA_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that
+ * loads the library holds it until the process exits.  The call allocates nothing.
+ *   Arguments: as kda_prefill_chunked, minus workspace and workspace_bytes.
+ *   Limit: a problem whose kda_prefill_workspace_bytes() exceeds KDA_NOALLOC_SCRATCH_BYTES returns
+ *   KDA_ERR_WORKSPACE without launching (64 MiB holds, e.g., one 512-token sequence at H = 32, dk = dv = 128).
+ *   The first call on a device resolves the array's device address (cudaGetSymbolAddress) with that
+ *   device current; make that first call before any stream capture on the device.
+ *   All calls on a device share the one array and it keeps the last call's contents (nothing in it needs
+ *   to start at zero): calls whose executions overlap on the GPU -- on different streams, or from
+ *   different host threads -- race on it and must be serialised by the caller.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u << 20)
+KDA_API int kda_prefill_chunked_noalloc(const kda_pool *pool, const kda_params *prm, int32_t nseq,
+                                        int64_t total_tokens, const int32_t *cu_seqlens, const int64_t *start_pos,
+                                        const int32_t *src_slot, const int32_t *dst_slot, int32_t chunk,
+                                        int64_t ckpt_interval, const int32_t *ckpt_offsets,
+                                        const int32_t *ckpt_slots, const uint16_t *q, const uint16_t *k,
+                                        const uint16_t *v, const uint16_t *a, const uint16_t *b, const uint16_t *z,
+                                        uint16_t *y, int32_t *dev_status, kda_stream_t stream);
+
+/*
  * Copy-on-write resume ("The Hardest Part: Prefix Caching for KDA": a cached partial state is copied
  * into a private destination before the request extends it): for each of n pairs, slot dst_slot[i]
  * receives a bit-exact copy of slot src_slot[i] (state and conv window, all heads).  src_slot and

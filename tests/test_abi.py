@@ -89,3 +89,10 @@ def test_binding_argument_counts_match_header(lib):
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         argtypes = getattr(lib, name).argtypes or []
         assert len(argtypes) == len(params), (name, len(argtypes), len(params))
+
+
+def test_noalloc_scratch_size_matches_header():
+    import hybrid_linear_attention_decode_gb300 as kda
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    m = re.search(r"#define KDA_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", src)
+    assert m and int(m.group(1)) << int(m.group(2)) == kda.NOALLOC_SCRATCH_BYTES
