@@ -396,7 +396,7 @@ def prefill_problem(seed: int, lens, chunk: int, interval: int, num_slots: int):
 
 
 def run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
-    T, cu, sp, dst, offs, ck = prefill_problem(seed, PRE_LENS, PRE_CHUNK, PRE_INTERVAL, DEC_SLOTS)
+    T, cu, sp, dst, offs, ck = prefill_problem(seed, PRE_LENS, PRE_CHUNK, PRE_INTERVAL, int(pool.S.shape[0]))
     tok = ki.token_inputs(seed + 1, T, H, DK, DV)
     d = {k: bf16_dev(v, dev) for k, v in tok.items()}
     y = torch.empty(T, H, DV, dtype=torch.bfloat16, device=dev)
@@ -427,6 +427,8 @@ def run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
         ms = max_over_ranks(e0.elapsed_time(e1), ws) / Kp
     except kda.KdaError as e:
         return {"error": str(e)}
+    if int(status.item()) != 0:
+        return {"error": f"device status {int(status.item())}"}
     io = PREFILL_IO_BYTES_PER_HEAD_TOKEN * T * H + CKPT_BYTES * int(offs[-1]) * H + len(PRE_LENS) * H * CKPT_BYTES
     return {"workload": "chunked prefill: 4 sequences of 2048/4096/8192/8192 tokens from empty prefixes, H=32, "
                         "dk=dv=128, chunk 64, checkpoints every 128 tokens (176 x 32 heads) into pool slots",

@@ -24,6 +24,7 @@
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
+#include "kda_umma.cuh"
 
 namespace kda {
 
@@ -450,6 +451,605 @@ __global__ void __launch_bounds__(kThreads) prefill_out_kernel(const PrefillArgs
     }
 }
 
+// ================================================================================ tensor-core path
+// dk = dv = 128, chunk 64.  Transposed formulation so that every MMA has M = 128 (TMEM lane = row):
+//   [A ; Qk]  = [K+ ; Q+] (mid-chunk reference) x K-^T           bf16, M=128 N=64  K=128
+//   W^T       = (k*exp(G))^T x T^T,   U'^T = V^T x T^T            tf32, M=128 N=64  K=64
+//   U^T       = U'^T + S^T x (-W)^T                                bf16, M=128 N=64  K=128
+//   O^T       = S^T x Q+^T + U^T x Qk^T                            bf16, M=128 N=64  K=128 / 64
+//   S^T       = S^T Diag(exp(G_last)) + U^T x Ktil                 tf32, M=128 N=128 K=64
+// tf32 operands are rounded to nearest (cvt.rna); accumulation is fp32 in tensor memory.
+namespace tc {
+
+constexpr int D = 128, CH = 64, NT = 256;
+constexpr float kMidRange = 40.f;  // |G_r - G_mid| bound for the factorised A / Qk (fp32-safe)
+
+// Workspace block per (chunk, head); the first WS_OPS bytes are operand tiles in their shared-memory
+// layout (K-major, 128B swizzle), copied verbatim by the state kernel.
+constexpr uint32_t WS_QK = 0;                    // bf16 [64 r][64 s]    Qk (scaled, masked)
+constexpr uint32_t WS_W = WS_QK + CH * CH * 2;   // bf16 [64 r][128 i]   -W (negated)
+constexpr uint32_t WS_QP = WS_W + CH * D * 2;    // bf16 [64 r][128 i]   scale * q * exp(G)
+constexpr uint32_t WS_KT = WS_QP + CH * D * 2;   // tf32 [128 i][64 r]   k * exp(G_last - G), transposed
+constexpr uint32_t WS_GL = WS_KT + D * CH * 4;   // fp32 [128]           exp(G_last)
+constexpr uint32_t WS_OPS = WS_GL + D * 4;
+constexpr uint32_t WS_UP = (WS_OPS + 255) / 256 * 256;  // fp32 [64 r][128 j]   U'
+constexpr uint32_t WS_BLOCK = WS_UP + CH * D * 4;
+static_assert(WS_W % 1024 == 0 && WS_QP % 1024 == 0 && WS_KT % 1024 == 0 && WS_GL % 1024 == 0, "tile align");
+static_assert(WS_OPS % 16 == 0, "bulk copy size");
+
+struct Layout2 {
+    int64_t maxc;
+    size_t off_cnt, off_ent, off_pos, off_seqc, off_flags, off_blk, total;
+};
+
+inline Layout2 make_layout2(int H, int nseq, int64_t T) {
+    Layout2 L;
+    L.maxc = T / CH + 2 * (int64_t)nseq + 1;
+    size_t o = 0;
+    L.off_cnt = o; o = align256(o + 16);
+    L.off_ent = o; o = align256(o + sizeof(ChunkEnt) * L.maxc);
+    L.off_pos = o; o = align256(o + sizeof(int64_t) * L.maxc);
+    L.off_seqc = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
+    L.off_flags = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
+    o = (o + 1023) & ~size_t(1023);
+    L.off_blk = o; o += (size_t)WS_BLOCK * L.maxc * H;
+    L.total = o;
+    return L;
+}
+
+inline Layout as_layout(const Layout2 &L2) {  // the table kernel only uses these fields
+    Layout L{};
+    L.maxc = L2.maxc;
+    L.off_cnt = L2.off_cnt; L.off_ent = L2.off_ent; L.off_pos = L2.off_pos;
+    L.off_seqc = L2.off_seqc; L.off_flags = L2.off_flags;
+    return L;
+}
+
+__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __syncthreads_or(!ok) == 0;
+}
+
+// Intra-chunk kernel smem (bytes, from a 1024-aligned base):
+constexpr uint32_t I_R0 = 0;          // q^ fp32 [64][128]          -> V^T tf32 tile [128 x 64]
+constexpr uint32_t I_R1 = 32768;      // k^ fp32 [64][128]          -> W bf16 tile staging
+constexpr uint32_t I_R2 = 65536;      // v  fp32 [64][128]          -> (k exp G)^T tf32 tile [128 x 64]
+constexpr uint32_t I_R3 = 98304;      // G  fp32 [64][128]          -> U' fp32 staging [64][128]
+constexpr uint32_t I_R4 = 131072;     // [K+;Q+] bf16 [128 x 128]   -> A fp32 [64][64] | Inv fp32 [64][64]
+constexpr uint32_t I_R5 = 163840;     // K- bf16 [64 x 128]         -> block temps, then T tf32 [64 x 64]
+constexpr uint32_t I_MISC = 180224;   // beta[64], flags, barrier, tmem address
+constexpr uint32_t I_SMEM = I_MISC + 1024 + 1024;  // + alignment slack
+
+__global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillArgs a, const Layout2 L) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int H = a.H, CC = 3 * D;
+    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (c >= *wsp<int32_t>(a, L.off_cnt)) return;
+    const ChunkEnt e = wsp<ChunkEnt>(a, L.off_ent)[c];
+    const int64_t p0 = wsp<int64_t>(a, L.off_pos)[c];
+    const int n = e.seq, ntok = e.n;
+    const int64_t start = a.start_pos[n], ts = a.cu_seqlens[n];
+    const int64_t len = (int64_t)a.cu_seqlens[n + 1] - ts;
+    const int srcv = a.src[n];
+
+    float *qh = reinterpret_cast<float *>(sm + I_R0);
+    float *kh = reinterpret_cast<float *>(sm + I_R1);
+    float *vv = reinterpret_cast<float *>(sm + I_R2);
+    float *G = reinterpret_cast<float *>(sm + I_R3);
+    float *beta = reinterpret_cast<float *>(sm + I_MISC);
+    int *flag_s = reinterpret_cast<int *>(sm + I_MISC + 256);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + I_MISC + 512);
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + I_MISC + 576);
+    uint8_t *blk = reinterpret_cast<uint8_t *>(a.ws) + L.off_blk + ((size_t)c * H + h) * WS_BLOCK;
+
+    if (warp == 0) umma::alloc(tmem_s, 256);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+
+    // ---- P1: causal conv + SiLU, gates, norms, cumulative log decay (as the SIMT path) ----
+    for (int ch = tid; ch < CC; ch += NT) {
+        float hist[kConvW - 1];
+        for (int j = 0; j < kConvW - 1; ++j)
+            hist[j] = bf2f(raw_at(a, D, D, h, ch, p0 - (kConvW - 1) + j, start, ts, srcv));
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
+        for (int r = 0; r < CH; ++r) {
+            float out = 0.f;
+            if (r < ntok) {
+                const float x = raw_input(a, D, D, e.t0 + r, h, ch);
+                out = w.w * x;
+                out = fmaf(w.x, hist[0], out);
+                out = fmaf(w.y, hist[1], out);
+                out = fmaf(w.z, hist[2], out);
+                if (a.silu) out = out / (1.f + __expf(-out));
+                hist[0] = hist[1];
+                hist[1] = hist[2];
+                hist[2] = x;
+            }
+            if (ch < D) qh[r * D + ch] = out;
+            else if (ch < 2 * D) kh[r * D + ch - D] = out;
+            else vv[r * D + ch - 2 * D] = out;
+        }
+    }
+    for (int idx = tid; idx < CH * D; idx += NT) {
+        const int r = idx >> 7, i = idx & 127;
+        G[idx] = r < ntok ? log_sigmoid(bf2f(a.a[((size_t)(e.t0 + r) * H + h) * D + i])) : 0.f;
+    }
+    for (int r = tid; r < CH; r += NT) beta[r] = r < ntok ? sigmoidf_(bf2f(a.b[(size_t)(e.t0 + r) * H + h])) : 0.f;
+    __syncthreads();
+    for (int r = warp; r < ntok; r += NT / 32) {
+        const float nq = warp_dot_array(qh + r * D, qh + r * D, D);
+        const float nk = warp_dot_array(kh + r * D, kh + r * D, D);
+        const float rq = rsqrtf(nq + a.l2_eps), rk = rsqrtf(nk + a.l2_eps);
+        for (int i = lane; i < D; i += 32) {
+            qh[r * D + i] *= rq;
+            kh[r * D + i] *= rk;
+        }
+    }
+    if (tid < D) {
+        float acc = 0.f;
+        for (int r = 0; r < CH; ++r) {
+            acc += G[r * D + tid];
+            G[r * D + tid] = acc;
+        }
+    }
+    __syncthreads();
+
+    // ---- P2: operands of [A ; Qk], workspace tiles Q+, Ktil^T, gl ----
+    constexpr int MID = CH / 2;
+    bool wide = false;
+    if (tid < D) {
+        const float g0 = G[tid], gm = G[MID * D + tid], gl = G[(CH - 1) * D + tid];
+        wide = (g0 - gm > kMidRange) || (gm - gl > kMidRange);
+    }
+    const bool slow = __syncthreads_or(wide) != 0;
+    uint8_t *X1 = sm + I_R4;
+    uint8_t *Km = sm + I_R5;
+    for (int idx = tid; idx < CH * D; idx += NT) {
+        const int r = idx >> 7, i = idx & 127;
+        const float g = G[idx], gm = G[MID * D + i], glast = G[(CH - 1) * D + i];
+        const float k_ = kh[idx], q_ = qh[idx];
+        if (!slow) {
+            const float ep = __expf(g - gm), em = __expf(gm - g);
+            umma::st_bf16(X1, 128, r, i, k_ * ep);
+            umma::st_bf16(X1, 128, CH + r, i, q_ * ep);
+            umma::st_bf16(Km, CH, r, i, k_ * em);
+        }
+        // Q+ (bf16 [64 r][128 i]) and Ktil^T (tf32 [128 i][64 r]) straight into the workspace tiles
+        *reinterpret_cast<__nv_bfloat16 *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, i)) =
+            __float2bfloat16_rn(a.scale * q_ * expf(g));
+        *reinterpret_cast<uint32_t *>(blk + WS_KT + umma::sw128_offset<4>(D, i, r)) = umma::to_tf32(k_ * expf(glast - g));
+    }
+    if (tid < D) reinterpret_cast<float *>(blk + WS_GL)[tid] = expf(G[(CH - 1) * D + tid]);
+    fence_proxy_async_smem();
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *tmem_s;
+    uint32_t phase = 0;
+    bool ok = true;
+    if (!slow) {
+        if (tid == 0) {
+            const uint32_t id = umma::idesc(umma::kBF16, 128, CH);
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma::mma_bf16(tmem, umma::sdesc_k(X1, 128, ks), umma::sdesc_k(Km, CH, ks), id, ks > 0);
+            umma::commit(bar);
+        }
+        ok = wait_all(bar, phase);
+        phase ^= 1;
+        umma::fence_after();
+    }
+    // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with diagonal, bf16 tile) ----
+    float *A = reinterpret_cast<float *>(sm + I_R4);          // [64][64]
+    float *Inv = reinterpret_cast<float *>(sm + I_R4 + 16384); // [64][64]
+    if (ok && !slow) {
+        const int quad = warp & 3, half = warp >> 2;          // lanes 32*quad.., columns 32*half..
+        float v[32];
+        umma::ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * half, v);
+        const int row = 32 * quad + lane;
+        __syncthreads();  // every warp has read D1: X1 may be overwritten
+        if (row < CH) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int s = 32 * half + j;
+                A[row * CH + s] = s < row ? v[j] : 0.f;
+            }
+        } else {
+            const int r = row - CH;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int s = 32 * half + j;
+                *reinterpret_cast<__nv_bfloat16 *>(blk + WS_QK + umma::sw128_offset<2>(CH, r, s)) =
+                    __float2bfloat16_rn(s <= r ? a.scale * v[j] : 0.f);
+            }
+        }
+    } else if (ok) {
+        // decay range too wide for one reference point: exact pairwise exponentials
+        for (int idx = tid; idx < CH * CH; idx += NT) {
+            const int r = idx / CH, s = idx - (idx / CH) * CH;
+            float accA = 0.f, accQ = 0.f;
+            if (s <= r && r < ntok) {
+                for (int i = 0; i < D; ++i) {
+                    const float dd = __expf(G[r * D + i] - G[s * D + i]);
+                    const float ks = kh[s * D + i] * dd;
+                    accA = fmaf(kh[r * D + i], ks, accA);
+                    accQ = fmaf(qh[r * D + i], ks, accQ);
+                }
+            }
+            A[idx] = s < r ? accA : 0.f;
+            *reinterpret_cast<__nv_bfloat16 *>(blk + WS_QK + umma::sw128_offset<2>(CH, r, s)) =
+                __float2bfloat16_rn(s <= r ? a.scale * accQ : 0.f);
+        }
+    }
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+        if (warp == 0) umma::dealloc(tmem, 256);
+        return;
+    }
+    // ---- P4: T = (I + diag(beta) A)^{-1} diag(beta), blocked by 16 ----
+    // L = I + diag(beta) A; Inv = L^{-1}.  Diagonal 16x16 blocks by substitution, one column per thread.
+    if (tid < CH) {
+        const int b = tid >> 4, col = tid & 15, base = 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = (r == col) ? 1.f : 0.f;
+            const float br = beta[base + r];
+#pragma unroll
+            for (int s = 0; s < r; ++s) acc = fmaf(-br * A[(base + r) * CH + base + s], x[s], acc);
+            x[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Inv[(base + r) * CH + base + col] = x[r];
+    }
+    // zero the strictly-upper blocks once
+    for (int idx = tid; idx < CH * CH; idx += NT) {
+        const int r = idx / CH, s = idx - (idx / CH) * CH;
+        if ((s >> 4) > (r >> 4)) Inv[idx] = 0.f;
+    }
+    __syncthreads();
+    float *P = reinterpret_cast<float *>(sm + I_R5);  // [3][16][16] temporaries (K- is dead)
+    for (int d = 1; d < 4; ++d) {
+        const int nb = 4 - d;  // blocks (i, i-d) for i = d..3
+        // P_i = sum_{k=i-d}^{i-1} L_ik Inv_k,(i-d)
+        for (int idx = tid; idx < nb * 256; idx += NT) {
+            const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+            const int i = bi + d, j = i - d;
+            const float br = beta[16 * i + rr];
+            float acc = 0.f;
+            for (int k = j; k < i; ++k)
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    acc = fmaf(br * A[(16 * i + rr) * CH + 16 * k + t], Inv[(16 * k + t) * CH + 16 * j + cc], acc);
+            P[idx] = acc;
+        }
+        __syncthreads();
+        // Inv_ij = -Inv_ii P_i
+        for (int idx = tid; idx < nb * 256; idx += NT) {
+            const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+            const int i = bi + d, j = i - d;
+            float acc = 0.f;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) acc = fmaf(Inv[(16 * i + rr) * CH + 16 * i + t], P[bi * 256 + t * 16 + cc], acc);
+            Inv[(16 * i + rr) * CH + 16 * j + cc] = -acc;
+        }
+        __syncthreads();
+    }
+    uint8_t *Tt = sm + I_R5;  // T tf32 [64 r][64 s]: the B operand of W^T = K+^T T^T (K-major: row r, K = s)
+    for (int idx = tid; idx < CH * CH; idx += NT) {
+        const int r = idx / CH, s = idx - (idx / CH) * CH;
+        umma::st_tf32(Tt, CH, r, s, Inv[idx] * beta[s]);
+    }
+    // ---- P5: A operands V^T (into R0) then (k exp G)^T (into R2, after V^T has read v) ----
+    uint8_t *Vt = sm + I_R0;
+    for (int idx = tid; idx < CH * D; idx += NT) {
+        const int j = idx >> 6, r = idx & 63;  // r fastest: one 256-byte row of the tile per 64 threads
+        umma::st_tf32(Vt, D, j, r, vv[r * D + j]);
+    }
+    __syncthreads();
+    uint8_t *Kpt = sm + I_R2;
+    for (int idx = tid; idx < CH * D; idx += NT) {
+        const int i = idx >> 6, r = idx & 63;
+        umma::st_tf32(Kpt, D, i, r, kh[r * D + i] * expf(G[r * D + i]));
+    }
+    fence_proxy_async_smem();
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    if (tid == 0) {
+        const uint32_t id = umma::idesc(umma::kTF32, 128, CH);
+        for (int ks = 0; ks < CH / 8; ++ks) {
+            const uint64_t bt = umma::sdesc_k(Tt, CH, ks);
+            umma::mma_tf32(tmem + 64, umma::sdesc_k(Kpt, D, ks), bt, id, ks > 0);
+            umma::mma_tf32(tmem + 128, umma::sdesc_k(Vt, D, ks), bt, id, ks > 0);
+        }
+        umma::commit(bar);
+    }
+    ok = wait_all(bar, phase);
+    phase ^= 1;
+    umma::fence_after();
+    if (!ok) {
+        if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+        if (warp == 0) umma::dealloc(tmem, 256);
+        return;
+    }
+    // ---- P6: W (bf16 tile [64 r][128 i]) and U' (fp32 [64 r][128 j]) via smem staging ----
+    uint8_t *Wst = sm + I_R1;
+    float *Ust = reinterpret_cast<float *>(sm + I_R3);
+    {
+        const int quad = warp & 3, half = warp >> 2;
+        const int row = 32 * quad + lane;  // channel i (for W^T) / j (for U'^T)
+        float v[32];
+        umma::ld32(tmem + ((uint32_t)(32 * quad) << 16) + 64 + 32 * half, v);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) umma::st_bf16(Wst, CH, 32 * half + t, row, -v[t]);
+        umma::ld32(tmem + ((uint32_t)(32 * quad) << 16) + 128 + 32 * half, v);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) Ust[(32 * half + t) * D + row] = v[t];
+    }
+    umma::fence_before();
+    __syncthreads();
+    {
+        const uint4 *s1 = reinterpret_cast<const uint4 *>(Wst);
+        uint4 *d1 = reinterpret_cast<uint4 *>(blk + WS_W);
+        for (int idx = tid; idx < CH * D * 2 / 16; idx += NT) d1[idx] = s1[idx];
+        const uint4 *s2 = reinterpret_cast<const uint4 *>(Ust);
+        uint4 *d2 = reinterpret_cast<uint4 *>(blk + WS_UP);
+        for (int idx = tid; idx < CH * D * 4 / 16; idx += NT) d2[idx] = s2[idx];
+    }
+    if (warp == 0) umma::dealloc(tmem, 256);
+
+    // raw conv windows at a checkpoint boundary / at the sequence end (as the SIMT path)
+    const int32_t flag = wsp<int32_t>(a, L.off_flags)[n];
+    const int64_t pend = p0 + ntok;
+    int wslot[2] = {-1, -1};
+    if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
+        const int64_t j = pend / a.interval - start / a.interval - 1;
+        const int s = a.ckpt_slots[a.ckpt_offsets[n] + j];
+        if (s >= a.num_slots || s < -1) {
+            if (tid == 0) set_status(a.status, KDA_DEV_BAD_SLOT);
+        } else {
+            wslot[0] = s;
+        }
+    }
+    if (pend == start + len) wslot[1] = a.dst[n];
+    for (int w = 0; w < 2; ++w) {
+        if (wslot[w] < 0) continue;
+        uint16_t *cw = a.conv + ((size_t)wslot[w] * H + h) * (kConvW - 1) * CC;
+        for (int idx = tid; idx < (kConvW - 1) * CC; idx += NT) {
+            const int row = idx / CC, ch = idx - (idx / CC) * CC;
+            cw[idx] = raw_at(a, D, D, h, ch, pend - (kConvW - 1) + row, start, ts, srcv);
+        }
+    }
+    (void)flag_s;
+}
+
+}  // namespace tc
+
+namespace tc {
+
+// State kernel smem (bytes, from a 1024-aligned base)
+constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand of U^T -= S^T W^T, O^T = S^T Q+^T
+constexpr uint32_t S_OPS = 32768;     // one chunk's operand tiles, WS_OPS bytes (Qk, W, Q+, Ktil^T, gl)
+constexpr uint32_t S_UT32 = 108544;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil
+constexpr uint32_t S_UT16 = 141312;   // U^T bf16 tile [128 j][64 r]: A operand of O^T += U^T Qk^T
+constexpr uint32_t S_OST = 157696;    // O staging fp32 [64 r][129]
+constexpr uint32_t S_MISC = 190720;   // barriers, tensor-memory address
+constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
+static_assert(S_OPS + WS_OPS <= S_UT32 && S_UT32 % 1024 == 0 && S_UT16 % 1024 == 0, "state smem layout");
+
+// TMEM columns: S^T [0,128), U^T [128,192), O^T [192,256)
+constexpr uint32_t T_S = 0, T_U = 128, T_O = 192;
+
+__global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillArgs a, const Layout2 L) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int H = a.H, CC = 3 * D;
+    const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t flag = wsp<int32_t>(a, L.off_flags)[n];
+    if (flag & kSeqInvalid) return;
+    const int src = a.src[n], dst = a.dst[n];  // validated by the table kernel
+    const int quad = warp & 3, half = warp >> 2;
+    const int j = 32 * quad + lane;            // this thread's value channel = tensor-memory lane
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    uint8_t *Sst = sm + S_ST;
+    uint8_t *ops = sm + S_OPS;
+    uint8_t *Ut32 = sm + S_UT32;
+    uint8_t *Ut16 = sm + S_UT16;
+    float *Ost = reinterpret_cast<float *>(sm + S_OST);
+    uint64_t *bar_ops = reinterpret_cast<uint64_t *>(sm + S_MISC);
+    uint64_t *bar_mma = bar_ops + 1;
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
+    const int64_t start = a.start_pos[n];
+    const int32_t c0 = wsp<int32_t>(a, L.off_seqc)[n], c1 = wsp<int32_t>(a, L.off_seqc)[n + 1];
+    const ChunkEnt *ent = wsp<ChunkEnt>(a, L.off_ent);
+    const int64_t *pos = wsp<int64_t>(a, L.off_pos);
+    const uint8_t *blk0 = reinterpret_cast<const uint8_t *>(a.ws) + L.off_blk;
+    auto blk_of = [&](int32_t c) { return blk0 + ((size_t)c * H + h) * WS_BLOCK; };
+
+    if (warp == 0) umma::alloc(tmem_s, 256);
+    if (tid == 0) {
+        mbar_init(bar_ops, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        if (c0 < c1) {
+            mbar_arrive_expect_tx(bar_ops, WS_OPS);
+            bulk_g2s(ops, blk_of(c0), WS_OPS, bar_ops);
+        }
+    }
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *tmem_s;
+
+    // initial state: S^T in tensor memory (lane j, column i) and its bf16 operand tile
+    {
+        float v[32];
+        for (int part = 0; part < 2; ++part) {
+            const int i0 = 64 * half + 32 * part;
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+                v[t] = src >= 0 ? a.S[(((size_t)src * H + h) * D + i0 + t) * D + j] : 0.f;
+            umma::st32(tmem + lane_off + T_S + i0, v);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) umma::st_bf16(Sst, D, j, i0 + t, v[t]);
+        }
+    }
+    uint32_t ph_ops = 0, ph_mma = 0;
+    bool ok = true;
+    for (int32_t c = c0; c < c1 && ok; ++c) {
+        const ChunkEnt e = ent[c];
+        const uint8_t *blk = blk_of(c);
+        // U' -> U^T columns of tensor memory (lane j, column r)
+        {
+            float v[32];
+            const float *up = reinterpret_cast<const float *>(blk + WS_UP);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) v[t] = up[(32 * half + t) * D + j];
+            umma::st32(tmem + lane_off + T_U + 32 * half, v);
+        }
+        fence_proxy_async_smem();
+        umma::fence_before();
+        __syncthreads();
+        umma::fence_after();
+        ok = mbar_wait(bar_ops, ph_ops);
+        ph_ops ^= 1;
+        if (tid == 0 && ok) {
+            const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t as = umma::sdesc_k(Sst, D, ks);
+                umma::mma_bf16(tmem + T_U, as, umma::sdesc_k(ops + WS_W, CH, ks), idp, true);   // U^T += S^T (-W)^T
+                umma::mma_bf16(tmem + T_O, as, umma::sdesc_k(ops + WS_QP, CH, ks), idp, ks > 0); // O^T = S^T Q+^T
+            }
+            umma::commit(bar_mma);
+        }
+        ok = __syncthreads_or(!ok) == 0 && wait_all(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        umma::fence_after();
+        if (!ok) break;
+        // U^T -> its tf32 and bf16 operand tiles; decay the state columns by exp(G_last)
+        {
+            float v[32];
+            umma::ld32(tmem + lane_off + T_U + 32 * half, v);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                umma::st_tf32(Ut32, D, j, 32 * half + t, v[t]);
+                umma::st_bf16(Ut16, D, j, 32 * half + t, v[t]);
+            }
+            const float *gl = reinterpret_cast<const float *>(ops + WS_GL);
+            for (int part = 0; part < 2; ++part) {
+                const int i0 = 64 * half + 32 * part;
+                umma::ld32(tmem + lane_off + T_S + i0, v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] *= gl[i0 + t];
+                umma::st32(tmem + lane_off + T_S + i0, v);
+            }
+        }
+        fence_proxy_async_smem();
+        umma::fence_before();
+        __syncthreads();
+        umma::fence_after();
+        if (tid == 0) {
+            const uint32_t ido = umma::idesc(umma::kBF16, 128, CH);
+            for (int ks = 0; ks < CH / 16; ++ks)  // O^T += U^T Qk^T
+                umma::mma_bf16(tmem + T_O, umma::sdesc_k(Ut16, D, ks), umma::sdesc_k(ops + WS_QK, CH, ks), ido, true);
+            const uint32_t ids = umma::idesc(umma::kTF32, 128, D);
+            for (int ks = 0; ks < CH / 8; ++ks)   // S^T += U^T Ktil
+                umma::mma_tf32(tmem + T_S, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_KT, D, ks), ids, true);
+            umma::commit(bar_mma);
+        }
+        ok = wait_all(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        umma::fence_after();
+        if (!ok) break;
+        // the operand buffer is free: start the next chunk's copy
+        if (tid == 0 && c + 1 < c1) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar_ops, WS_OPS);
+            bulk_g2s(ops, blk_of(c + 1), WS_OPS, bar_ops);
+        }
+        // outputs: O^T -> staging -> gated RMSNorm -> y
+        {
+            float v[32];
+            umma::ld32(tmem + lane_off + T_O + 32 * half, v);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) Ost[(32 * half + t) * 129 + j] = v[t];
+        }
+        __syncthreads();
+        {
+            const int r = tid >> 2, part = tid & 3;  // 4 threads per token, 32 channels each
+            float ss = 0.f;
+#pragma unroll 8
+            for (int t = 0; t < 32; ++t) {
+                const float o = Ost[r * 129 + 32 * part + t];
+                ss = fmaf(o, o, ss);
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            const float rr = rsqrtf(ss * (1.0f / D) + a.rms_eps);
+            if (r < e.n) {
+                const size_t base = ((size_t)(e.t0 + r) * H + h) * D + 32 * part;
+                for (int t = 0; t < 32; t += 2) {
+                    const int jj = 32 * part + t;
+                    float y0 = Ost[r * 129 + jj] * rr * __ldg(a.norm_w + jj);
+                    float y1 = Ost[r * 129 + jj + 1] * rr * __ldg(a.norm_w + jj + 1);
+                    if (a.z) {
+                        const uint32_t zz = *reinterpret_cast<const uint32_t *>(a.z + base + t);
+                        y0 *= sigmoidf_(bf2f((uint16_t)(zz & 0xffff)));
+                        y1 *= sigmoidf_(bf2f((uint16_t)(zz >> 16)));
+                    }
+                    *reinterpret_cast<uint32_t *>(a.y + base + t) = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
+                }
+            }
+        }
+        // new state: bf16 operand tile for the next chunk; checkpoint when this chunk ends on a boundary
+        const int64_t pend = pos[c] + e.n;
+        int ck = -1;
+        if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
+            const int64_t jj = pend / a.interval - start / a.interval - 1;
+            const int s = a.ckpt_slots[a.ckpt_offsets[n] + jj];
+            if (s >= 0 && s < a.num_slots) ck = s;
+        }
+        {
+            float v[32];
+            for (int part = 0; part < 2; ++part) {
+                const int i0 = 64 * half + 32 * part;
+                umma::ld32(tmem + lane_off + T_S + i0, v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) umma::st_bf16(Sst, D, j, i0 + t, v[t]);
+                if (ck >= 0) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) a.S[(((size_t)ck * H + h) * D + i0 + t) * D + j] = v[t];
+                }
+            }
+        }
+        __syncthreads();  // staging and tiles are reused by the next chunk
+    }
+    if (!ok) {
+        if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+    } else {
+        float v[32];
+        for (int part = 0; part < 2; ++part) {
+            const int i0 = 64 * half + 32 * part;
+            umma::ld32(tmem + lane_off + T_S + i0, v);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) a.S[(((size_t)dst * H + h) * D + i0 + t) * D + j] = v[t];
+        }
+        if (c0 == c1) {  // empty sequence: the window passes through unchanged
+            uint16_t *cw = a.conv + ((size_t)dst * H + h) * (kConvW - 1) * CC;
+            for (int idx = tid; idx < (kConvW - 1) * CC; idx += NT)
+                cw[idx] = src >= 0 ? a.conv[((size_t)src * H + h) * (kConvW - 1) * CC + idx] : (uint16_t)0;
+        }
+    }
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) umma::dealloc(tmem, 256);
+}
+
+}  // namespace tc
+
 }  // namespace
 
 bool prefill_supported(int dk, int dv, int W, int chunk) {
@@ -457,11 +1057,39 @@ bool prefill_supported(int dk, int dv, int W, int chunk) {
     return decode_supported(dk, dv, W);
 }
 
+static bool use_tensor_cores(int dk, int dv, int chunk) { return dk == 128 && dv == 128 && chunk == 64; }
+
 size_t prefill_workspace_bytes(int H, int dk, int dv, int nseq, int64_t total_tokens, int chunk) {
+    if (use_tensor_cores(dk, dv, chunk)) return tc::make_layout2(H, nseq, total_tokens).total;
     return make_layout(H, dk, dv, nseq, total_tokens, chunk).total;
 }
 
+static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
+    const tc::Layout2 L2 = tc::make_layout2(a.H, a.nseq, a.total_tokens);
+    static int attr_done[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_CUDA;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(tc::prefill_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc::I_SMEM) != cudaSuccess ||
+            cudaFuncSetAttribute(tc::prefill_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc::S_SMEM) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        attr_done[dev] = 1;
+    }
+    if (L2.maxc > 0x7fffffffLL || a.H > 65535) return KDA_ERR_INVALID_ARG;
+    prefill_table_kernel<<<1, kMaxSeqThreads, 0, st>>>(a, tc::as_layout(L2));
+    if (a.total_tokens > 0) {
+        dim3 gi((unsigned)L2.maxc, a.H);
+        tc::prefill_intra_tc_kernel<<<gi, tc::NT, tc::I_SMEM, st>>>(a, L2);
+    }
+    dim3 gs(a.nseq, a.H);
+    tc::prefill_state_tc_kernel<<<gs, tc::NT, tc::S_SMEM, st>>>(a, L2);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st) {
+    if (use_tensor_cores(dk, dv, a.chunk)) return launch_prefill_tc(a, st);
     const Layout L = make_layout(a.H, dk, dv, a.nseq, a.total_tokens, a.chunk);
     const int C = a.chunk;
     const size_t smem_intra = sizeof(float) * (3 * C * dk + C * (dk + dv) + 2 * C * C + C);
