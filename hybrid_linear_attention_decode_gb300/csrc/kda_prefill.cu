@@ -510,15 +510,18 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
     return __syncthreads_or(!ok) == 0;
 }
 
-// Intra-chunk kernel smem (bytes, from a 1024-aligned base):
-constexpr uint32_t I_R0 = 0;          // q^ fp32 [64][128]          -> V^T tf32 tile [128 x 64]
-constexpr uint32_t I_R1 = 32768;      // k^ fp32 [64][128]          -> W bf16 tile staging
-constexpr uint32_t I_R2 = 65536;      // v  fp32 [64][128]          -> (k exp G)^T tf32 tile [128 x 64]
-constexpr uint32_t I_R3 = 98304;      // G  fp32 [64][128]          -> U' fp32 staging [64][128]
-constexpr uint32_t I_R4 = 131072;     // [K+;Q+] bf16 [128 x 128]   -> A fp32 [64][64] | Inv fp32 [64][64]
-constexpr uint32_t I_R5 = 163840;     // K- bf16 [64 x 128]         -> block temps, then T tf32 [64 x 64]
-constexpr uint32_t I_MISC = 180224;   // beta[64], flags, barrier, tmem address
-constexpr uint32_t I_SMEM = I_MISC + 1024 + 1024;  // + alignment slack
+// Intra-chunk kernel smem (bytes, from a 1024-aligned base), by phase:
+//   P0-P1  [0,32K) q^ fp32 | [32K,64K) k^ fp32 | [64K,96K) G fp32 | [96K,128K) V^T tf32 tile | [128K,180K) raw rows
+//   P2     [128K,160K) [K+;Q+] bf16 tile | [160K,176K) K- bf16 tile
+//   P3-P4  [0,8K) Qk staging | [128K,144K) A fp32 | [144K,160K) Inv fp32 | [160K,176K) block temps, then T tf32
+//   P5     [0,32K) (k exp G)^T tf32 tile | [128K,160K) Ktil^T tf32 staging
+//   P6     [32K,48K) -W bf16 staging | [64K,96K) U' fp32 staging
+constexpr uint32_t I_Q = 0, I_K = 32768, I_G = 65536, I_VT = 98304, I_RAW = 131072;
+constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_INV = 147456, I_T = 163840;
+constexpr uint32_t I_MISC = 184320;   // beta[64], exp(G_mid)[128], exp(G_last)[128], barrier, tensor-memory address
+constexpr uint32_t I_SMEM = I_MISC + 2048 + 1024;  // + alignment slack
+constexpr int RAW_ROWS = CH + kConvW - 1;           // 3 history rows + 64 tokens
+static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
 
 __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillArgs a, const Layout2 L) {
     extern __shared__ uint8_t smem_raw[];
@@ -533,14 +536,16 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     const int64_t len = (int64_t)a.cu_seqlens[n + 1] - ts;
     const int srcv = a.src[n];
 
-    float *qh = reinterpret_cast<float *>(sm + I_R0);
-    float *kh = reinterpret_cast<float *>(sm + I_R1);
-    float *vv = reinterpret_cast<float *>(sm + I_R2);
-    float *G = reinterpret_cast<float *>(sm + I_R3);
+    float *qh = reinterpret_cast<float *>(sm + I_Q);
+    float *kh = reinterpret_cast<float *>(sm + I_K);
+    float *G = reinterpret_cast<float *>(sm + I_G);
+    uint8_t *Vt = sm + I_VT;
+    uint16_t *raw = reinterpret_cast<uint16_t *>(sm + I_RAW);  // [67][384] bf16, row = position p0 - 3 + row
     float *beta = reinterpret_cast<float *>(sm + I_MISC);
-    int *flag_s = reinterpret_cast<int *>(sm + I_MISC + 256);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + I_MISC + 512);
-    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + I_MISC + 576);
+    float *eGm = beta + 64;     // exp(G_mid) per channel
+    float *eGl = eGm + D;       // exp(G_last - G_mid) per channel
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + I_MISC + 1536);
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + I_MISC + 1600);
     uint8_t *blk = reinterpret_cast<uint8_t *>(a.ws) + L.off_blk + ((size_t)c * H + h) * WS_BLOCK;
 
     if (warp == 0) umma::alloc(tmem_s, 256);
@@ -549,35 +554,58 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         fence_mbar_init();
     }
 
-    // ---- P1: causal conv + SiLU, gates, norms, cumulative log decay (as the SIMT path) ----
-    for (int ch = tid; ch < CC; ch += NT) {
-        float hist[kConvW - 1];
-        for (int j = 0; j < kConvW - 1; ++j)
-            hist[j] = bf2f(raw_at(a, D, D, h, ch, p0 - (kConvW - 1) + j, start, ts, srcv));
-        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
-        for (int r = 0; r < CH; ++r) {
-            float out = 0.f;
-            if (r < ntok) {
-                const float x = raw_input(a, D, D, e.t0 + r, h, ch);
-                out = w.w * x;
-                out = fmaf(w.x, hist[0], out);
-                out = fmaf(w.y, hist[1], out);
-                out = fmaf(w.z, hist[2], out);
-                if (a.silu) out = out / (1.f + __expf(-out));
-                hist[0] = hist[1];
-                hist[1] = hist[2];
-                hist[2] = x;
+    // ---- P0: the chunk's raw q|k|v rows (and 3 rows of history) into smem; decay logits; beta ----
+    for (int idx = tid; idx < RAW_ROWS * 48; idx += NT) {
+        const int row = idx / 48, part = idx - (idx / 48) * 48;  // 48 x 16 bytes per row: q 16, k 16, v 16
+        const int64_t p = p0 - (kConvW - 1) + row;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (row < (kConvW - 1) + ntok) {
+            if (p >= start) {
+                const size_t t = (size_t)(ts + (p - start)) * H + h;
+                const uint16_t *srcp = part < 16 ? a.q + t * D : (part < 32 ? a.k + t * D : a.v + t * D);
+                val = __ldg(reinterpret_cast<const uint4 *>(srcp) + (part & 15));
+            } else if (srcv >= 0) {
+                const int crow = (int)(p - start + (kConvW - 1));
+                val = __ldg(reinterpret_cast<const uint4 *>(a.conv + (((size_t)srcv * H + h) * (kConvW - 1) + crow) * CC) +
+                            part);
             }
-            if (ch < D) qh[r * D + ch] = out;
-            else if (ch < 2 * D) kh[r * D + ch - D] = out;
-            else vv[r * D + ch - 2 * D] = out;
         }
+        reinterpret_cast<uint4 *>(raw + row * CC)[part] = val;
     }
-    for (int idx = tid; idx < CH * D; idx += NT) {
-        const int r = idx >> 7, i = idx & 127;
-        G[idx] = r < ntok ? log_sigmoid(bf2f(a.a[((size_t)(e.t0 + r) * H + h) * D + i])) : 0.f;
+    for (int idx = tid; idx < CH * 16; idx += NT) {
+        const int r = idx >> 4, part = idx & 15;
+        float g8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (r < ntok) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.a + ((size_t)(e.t0 + r) * H + h) * D) + part);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                g8[2 * u] = log_sigmoid(bf2f((uint16_t)(w4[u] & 0xffff)));
+                g8[2 * u + 1] = log_sigmoid(bf2f((uint16_t)(w4[u] >> 16)));
+            }
+        }
+        float4 *gd = reinterpret_cast<float4 *>(G + r * D + part * 8);
+        gd[0] = make_float4(g8[0], g8[1], g8[2], g8[3]);
+        gd[1] = make_float4(g8[4], g8[5], g8[6], g8[7]);
     }
     for (int r = tid; r < CH; r += NT) beta[r] = r < ntok ? sigmoidf_(bf2f(a.b[(size_t)(e.t0 + r) * H + h])) : 0.f;
+    __syncthreads();
+    // ---- P1: causal conv + SiLU, token-parallel from smem; v goes straight into its V^T tile ----
+    for (int idx = tid; idx < CH * CC; idx += NT) {
+        const int r = idx / CC, ch = idx - (idx / CC) * CC;
+        float out = 0.f;
+        if (r < ntok) {
+            const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
+            out = w.w * bf2f(raw[(r + 3) * CC + ch]);
+            out = fmaf(w.x, bf2f(raw[r * CC + ch]), out);
+            out = fmaf(w.y, bf2f(raw[(r + 1) * CC + ch]), out);
+            out = fmaf(w.z, bf2f(raw[(r + 2) * CC + ch]), out);
+            if (a.silu) out = out / (1.f + __expf(-out));
+        }
+        if (ch < D) qh[r * D + ch] = out;
+        else if (ch < 2 * D) kh[r * D + ch - D] = out;
+        else umma::st_tf32(Vt, D, ch - 2 * D, r, out);
+    }
     __syncthreads();
     for (int r = warp; r < ntok; r += NT / 32) {
         const float nq = warp_dot_array(qh + r * D, qh + r * D, D);
@@ -597,30 +625,35 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     }
     __syncthreads();
 
-    // ---- P2: operands of [A ; Qk], workspace tiles Q+, Ktil^T, gl ----
+    // ---- P2: [K+;Q+] and K- with a mid-chunk reference; Q+ tile to the workspace ----
     constexpr int MID = CH / 2;
     bool wide = false;
     if (tid < D) {
         const float g0 = G[tid], gm = G[MID * D + tid], gl = G[(CH - 1) * D + tid];
         wide = (g0 - gm > kMidRange) || (gm - gl > kMidRange);
+        eGm[tid] = expf(gm);
+        eGl[tid] = expf(gl - gm);
     }
     const bool slow = __syncthreads_or(wide) != 0;
-    uint8_t *X1 = sm + I_R4;
-    uint8_t *Km = sm + I_R5;
+    uint8_t *X1 = sm + I_X1;
+    uint8_t *Km = sm + I_KM;
     for (int idx = tid; idx < CH * D; idx += NT) {
         const int r = idx >> 7, i = idx & 127;
-        const float g = G[idx], gm = G[MID * D + i], glast = G[(CH - 1) * D + i];
+        const float g = G[idx];
         const float k_ = kh[idx], q_ = qh[idx];
+        float eq;  // exp(G)
         if (!slow) {
-            const float ep = __expf(g - gm), em = __expf(gm - g);
+            const float ep = __expf(g - G[MID * D + i]);
+            const float em = __frcp_rn(ep);
             umma::st_bf16(X1, 128, r, i, k_ * ep);
             umma::st_bf16(X1, 128, CH + r, i, q_ * ep);
             umma::st_bf16(Km, CH, r, i, k_ * em);
+            eq = ep * eGm[i];
+        } else {
+            eq = __expf(g);
         }
-        // Q+ (bf16 [64 r][128 i]) and Ktil^T (tf32 [128 i][64 r]) straight into the workspace tiles
         *reinterpret_cast<__nv_bfloat16 *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, i)) =
-            __float2bfloat16_rn(a.scale * q_ * expf(g));
-        *reinterpret_cast<uint32_t *>(blk + WS_KT + umma::sw128_offset<4>(D, i, r)) = umma::to_tf32(k_ * expf(glast - g));
+            __float2bfloat16_rn(a.scale * q_ * eq);
     }
     if (tid < D) reinterpret_cast<float *>(blk + WS_GL)[tid] = expf(G[(CH - 1) * D + tid]);
     fence_proxy_async_smem();
@@ -642,45 +675,45 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         umma::fence_after();
     }
     // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with diagonal, bf16 tile) ----
-    float *A = reinterpret_cast<float *>(sm + I_R4);          // [64][64]
-    float *Inv = reinterpret_cast<float *>(sm + I_R4 + 16384); // [64][64]
+    float *A = reinterpret_cast<float *>(sm + I_A);      // [64][64]
+    float *Inv = reinterpret_cast<float *>(sm + I_INV);  // [64][64]
+    // Qk tile staging: over q^ (dead) on the fast path; the slow path still reads q^, so it stages in the
+    // Inv region, which P4 fills only after the copy-out below
+    uint8_t *Qks = slow ? sm + I_INV : sm + I_Q;
     if (ok && !slow) {
-        const int quad = warp & 3, half = warp >> 2;          // lanes 32*quad.., columns 32*half..
+        const int quad = warp & 3, half = warp >> 2;     // lanes 32*quad.., columns 32*half..
         float v[32];
         umma::ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * half, v);
         const int row = 32 * quad + lane;
-        __syncthreads();  // every warp has read D1: X1 may be overwritten
+        __syncthreads();  // every warp has read D1 and X1 is no longer read: A may overwrite it
         if (row < CH) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int s = 32 * half + j;
-                A[row * CH + s] = s < row ? v[j] : 0.f;
+            for (int t = 0; t < 32; ++t) {
+                const int s_ = 32 * half + t;
+                A[row * CH + s_] = s_ < row ? v[t] : 0.f;
             }
         } else {
             const int r = row - CH;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int s = 32 * half + j;
-                *reinterpret_cast<__nv_bfloat16 *>(blk + WS_QK + umma::sw128_offset<2>(CH, r, s)) =
-                    __float2bfloat16_rn(s <= r ? a.scale * v[j] : 0.f);
+            for (int t = 0; t < 32; ++t) {
+                const int s_ = 32 * half + t;
+                umma::st_bf16(Qks, CH, r, s_, s_ <= r ? a.scale * v[t] : 0.f);
             }
         }
     } else if (ok) {
         // decay range too wide for one reference point: exact pairwise exponentials
         for (int idx = tid; idx < CH * CH; idx += NT) {
-            const int r = idx / CH, s = idx - (idx / CH) * CH;
+            const int r = idx / CH, s_ = idx - (idx / CH) * CH;
             float accA = 0.f, accQ = 0.f;
-            if (s <= r && r < ntok) {
+            if (s_ <= r && r < ntok) {
                 for (int i = 0; i < D; ++i) {
-                    const float dd = __expf(G[r * D + i] - G[s * D + i]);
-                    const float ks = kh[s * D + i] * dd;
+                    const float ks = kh[s_ * D + i] * __expf(G[r * D + i] - G[s_ * D + i]);
                     accA = fmaf(kh[r * D + i], ks, accA);
                     accQ = fmaf(qh[r * D + i], ks, accQ);
                 }
             }
-            A[idx] = s < r ? accA : 0.f;
-            *reinterpret_cast<__nv_bfloat16 *>(blk + WS_QK + umma::sw128_offset<2>(CH, r, s)) =
-                __float2bfloat16_rn(s <= r ? a.scale * accQ : 0.f);
+            A[idx] = s_ < r ? accA : 0.f;
+            umma::st_bf16(Qks, CH, r, s_, s_ <= r ? a.scale * accQ : 0.f);
         }
     }
     if (__syncthreads_or(!ok)) {
@@ -688,6 +721,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         if (warp == 0) umma::dealloc(tmem, 256);
         return;
     }
+    {
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(Qks);
+        uint4 *d4 = reinterpret_cast<uint4 *>(blk + WS_QK);
+        for (int idx = tid; idx < CH * CH * 2 / 16; idx += NT) d4[idx] = s4[idx];
+    }
+    __syncthreads();
     // ---- P4: T = (I + diag(beta) A)^{-1} diag(beta), blocked by 16 ----
     // L = I + diag(beta) A; Inv = L^{-1}.  Diagonal 16x16 blocks by substitution, one column per thread.
     if (tid < CH) {
@@ -698,23 +737,21 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
             float acc = (r == col) ? 1.f : 0.f;
             const float br = beta[base + r];
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc = fmaf(-br * A[(base + r) * CH + base + s], x[s], acc);
+            for (int s_ = 0; s_ < r; ++s_) acc = fmaf(-br * A[(base + r) * CH + base + s_], x[s_], acc);
             x[r] = acc;
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Inv[(base + r) * CH + base + col] = x[r];
     }
-    // zero the strictly-upper blocks once
     for (int idx = tid; idx < CH * CH; idx += NT) {
-        const int r = idx / CH, s = idx - (idx / CH) * CH;
-        if ((s >> 4) > (r >> 4)) Inv[idx] = 0.f;
+        const int r = idx / CH, s_ = idx - (idx / CH) * CH;
+        if ((s_ >> 4) > (r >> 4)) Inv[idx] = 0.f;
     }
     __syncthreads();
-    float *P = reinterpret_cast<float *>(sm + I_R5);  // [3][16][16] temporaries (K- is dead)
+    float *P = reinterpret_cast<float *>(sm + I_T);  // [3][16][16] temporaries (K- is dead)
     for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;  // blocks (i, i-d) for i = d..3
-        // P_i = sum_{k=i-d}^{i-1} L_ik Inv_k,(i-d)
-        for (int idx = tid; idx < nb * 256; idx += NT) {
+        for (int idx = tid; idx < nb * 256; idx += NT) {  // P_i = sum_{k=i-d}^{i-1} L_ik Inv_k,(i-d)
             const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
             const int i = bi + d, j = i - d;
             const float br = beta[16 * i + rr];
@@ -726,8 +763,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
             P[idx] = acc;
         }
         __syncthreads();
-        // Inv_ij = -Inv_ii P_i
-        for (int idx = tid; idx < nb * 256; idx += NT) {
+        for (int idx = tid; idx < nb * 256; idx += NT) {  // Inv_ij = -Inv_ii P_i
             const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
             const int i = bi + d, j = i - d;
             float acc = 0.f;
@@ -737,22 +773,21 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         }
         __syncthreads();
     }
-    uint8_t *Tt = sm + I_R5;  // T tf32 [64 r][64 s]: the B operand of W^T = K+^T T^T (K-major: row r, K = s)
+    uint8_t *Tt = sm + I_T;  // T tf32 [64 r][64 s]: the B operand of W^T = K+^T T^T (K-major: row r, K = s)
     for (int idx = tid; idx < CH * CH; idx += NT) {
-        const int r = idx / CH, s = idx - (idx / CH) * CH;
-        umma::st_tf32(Tt, CH, r, s, Inv[idx] * beta[s]);
+        const int r = idx / CH, s_ = idx - (idx / CH) * CH;
+        umma::st_tf32(Tt, CH, r, s_, Inv[idx] * beta[s_]);
     }
-    // ---- P5: A operands V^T (into R0) then (k exp G)^T (into R2, after V^T has read v) ----
-    uint8_t *Vt = sm + I_R0;
+    __syncthreads();  // A / Inv are dead: Ktil^T may be staged over them
+    // ---- P5: (k exp G)^T tile (A operand) and the Ktil^T workspace tile ----
+    uint8_t *Kpt = sm + I_Q;
+    uint8_t *Kts = sm + I_A;
     for (int idx = tid; idx < CH * D; idx += NT) {
-        const int j = idx >> 6, r = idx & 63;  // r fastest: one 256-byte row of the tile per 64 threads
-        umma::st_tf32(Vt, D, j, r, vv[r * D + j]);
-    }
-    __syncthreads();
-    uint8_t *Kpt = sm + I_R2;
-    for (int idx = tid; idx < CH * D; idx += NT) {
-        const int i = idx >> 6, r = idx & 63;
-        umma::st_tf32(Kpt, D, i, r, kh[r * D + i] * expf(G[r * D + i]));
+        const int r = idx >> 7, i = idx & 127;
+        const float g = G[idx], k_ = kh[idx];
+        const float eq = __expf(g);
+        umma::st_tf32(Kpt, D, i, r, k_ * eq);
+        umma::st_tf32(Kts, D, i, r, slow ? k_ * __expf(G[(CH - 1) * D + i] - g) : k_ * eGl[i] * __frcp_rn(__expf(g - G[MID * D + i])));
     }
     fence_proxy_async_smem();
     umma::fence_before();
@@ -767,6 +802,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         }
         umma::commit(bar);
     }
+    {
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(Kts);
+        uint4 *d4 = reinterpret_cast<uint4 *>(blk + WS_KT);
+        for (int idx = tid; idx < D * CH * 4 / 16; idx += NT) d4[idx] = s4[idx];
+    }
     ok = wait_all(bar, phase);
     phase ^= 1;
     umma::fence_after();
@@ -775,9 +815,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         if (warp == 0) umma::dealloc(tmem, 256);
         return;
     }
-    // ---- P6: W (bf16 tile [64 r][128 i]) and U' (fp32 [64 r][128 j]) via smem staging ----
-    uint8_t *Wst = sm + I_R1;
-    float *Ust = reinterpret_cast<float *>(sm + I_R3);
+    // ---- P6: -W (bf16 tile [64 r][128 i]) and U' (fp32 [64 r][128 j]) via smem staging ----
+    uint8_t *Wst = sm + I_K;
+    float *Ust = reinterpret_cast<float *>(sm + I_G);
     {
         const int quad = warp & 3, half = warp >> 2;
         const int row = 32 * quad + lane;  // channel i (for W^T) / j (for U'^T)
@@ -806,12 +846,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     const int64_t pend = p0 + ntok;
     int wslot[2] = {-1, -1};
     if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
-        const int64_t j = pend / a.interval - start / a.interval - 1;
-        const int s = a.ckpt_slots[a.ckpt_offsets[n] + j];
-        if (s >= a.num_slots || s < -1) {
+        const int64_t jj = pend / a.interval - start / a.interval - 1;
+        const int s_ = a.ckpt_slots[a.ckpt_offsets[n] + jj];
+        if (s_ >= a.num_slots || s_ < -1) {
             if (tid == 0) set_status(a.status, KDA_DEV_BAD_SLOT);
         } else {
-            wslot[0] = s;
+            wslot[0] = s_;
         }
     }
     if (pend == start + len) wslot[1] = a.dst[n];
@@ -823,7 +863,6 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
             cw[idx] = raw_at(a, D, D, h, ch, pend - (kConvW - 1) + row, start, ts, srcv);
         }
     }
-    (void)flag_s;
 }
 
 }  // namespace tc
@@ -831,14 +870,16 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
 namespace tc {
 
 // State kernel smem (bytes, from a 1024-aligned base)
-constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand of U^T -= S^T W^T, O^T = S^T Q+^T
-constexpr uint32_t S_OPS = 32768;     // one chunk's operand tiles, WS_OPS bytes (Qk, W, Q+, Ktil^T, gl)
-constexpr uint32_t S_UT32 = 108544;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil
-constexpr uint32_t S_UT16 = 141312;   // U^T bf16 tile [128 j][64 r]: A operand of O^T += U^T Qk^T
-constexpr uint32_t S_OST = 157696;    // O staging fp32 [64 r][129]
-constexpr uint32_t S_MISC = 190720;   // barriers, tensor-memory address
+constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand of U^T += S^T (-W)^T, O^T = S^T Q+^T
+constexpr uint32_t S_OPS = 32768;     // one chunk's workspace block (Qk, -W, Q+, Ktil^T, gl, U'), WS_BLOCK bytes
+constexpr uint32_t S_UT32 = 140288;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil
+constexpr uint32_t S_UT16 = 173056;   // U^T bf16 tile [128 j][64 r]: A operand of O^T += U^T Qk^T
+constexpr uint32_t S_OST = 189440;    // O staging fp32 [64 r][129]
+constexpr uint32_t S_NW = 222464;     // RMSNorm weight [128]
+constexpr uint32_t S_MISC = 222976;   // barriers, tensor-memory address
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
-static_assert(S_OPS + WS_OPS <= S_UT32 && S_UT32 % 1024 == 0 && S_UT16 % 1024 == 0, "state smem layout");
+static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0 && S_UT16 % 1024 == 0, "state smem layout");
+static_assert(S_OST + CH * 129 * 4 <= S_NW, "state smem layout");
 
 // TMEM columns: S^T [0,128), U^T [128,192), O^T [192,256)
 constexpr uint32_t T_S = 0, T_U = 128, T_O = 192;
@@ -859,6 +900,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
     uint8_t *Ut32 = sm + S_UT32;
     uint8_t *Ut16 = sm + S_UT16;
     float *Ost = reinterpret_cast<float *>(sm + S_OST);
+    float *nw = reinterpret_cast<float *>(sm + S_NW);
     uint64_t *bar_ops = reinterpret_cast<uint64_t *>(sm + S_MISC);
     uint64_t *bar_mma = bar_ops + 1;
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
@@ -870,13 +912,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
     auto blk_of = [&](int32_t c) { return blk0 + ((size_t)c * H + h) * WS_BLOCK; };
 
     if (warp == 0) umma::alloc(tmem_s, 256);
+    for (int jj = tid; jj < D; jj += NT) nw[jj] = __ldg(a.norm_w + jj);
     if (tid == 0) {
         mbar_init(bar_ops, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         if (c0 < c1) {
-            mbar_arrive_expect_tx(bar_ops, WS_OPS);
-            bulk_g2s(ops, blk_of(c0), WS_OPS, bar_ops);
+            mbar_arrive_expect_tx(bar_ops, WS_BLOCK);
+            bulk_g2s(ops, blk_of(c0), WS_BLOCK, bar_ops);
         }
     }
     umma::fence_before();
@@ -901,11 +944,21 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
     bool ok = true;
     for (int32_t c = c0; c < c1 && ok; ++c) {
         const ChunkEnt e = ent[c];
-        const uint8_t *blk = blk_of(c);
+        // this thread's slice of the output gate, fetched early: token tid/4, channels 32*(tid%4)..
+        uint4 zr[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                       make_uint4(0u, 0u, 0u, 0u)};
+        if (a.z && (tid >> 2) < e.n) {
+            const uint4 *zp = reinterpret_cast<const uint4 *>(a.z + ((size_t)(e.t0 + (tid >> 2)) * H + h) * D +
+                                                              32 * (tid & 3));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) zr[u] = __ldg(zp + u);
+        }
+        ok = mbar_wait(bar_ops, ph_ops);
+        ph_ops ^= 1;
         // U' -> U^T columns of tensor memory (lane j, column r)
-        {
+        if (ok) {
             float v[32];
-            const float *up = reinterpret_cast<const float *>(blk + WS_UP);
+            const float *up = reinterpret_cast<const float *>(ops + WS_UP);
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] = up[(32 * half + t) * D + j];
             umma::st32(tmem + lane_off + T_U + 32 * half, v);
@@ -914,8 +967,6 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
         umma::fence_before();
         __syncthreads();
         umma::fence_after();
-        ok = mbar_wait(bar_ops, ph_ops);
-        ph_ops ^= 1;
         if (tid == 0 && ok) {
             const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
             for (int ks = 0; ks < D / 16; ++ks) {
@@ -967,8 +1018,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
         // the operand buffer is free: start the next chunk's copy
         if (tid == 0 && c + 1 < c1) {
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar_ops, WS_OPS);
-            bulk_g2s(ops, blk_of(c + 1), WS_OPS, bar_ops);
+            mbar_arrive_expect_tx(bar_ops, WS_BLOCK);
+            bulk_g2s(ops, blk_of(c + 1), WS_BLOCK, bar_ops);
         }
         // outputs: O^T -> staging -> gated RMSNorm -> y
         {
@@ -991,17 +1042,27 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
             const float rr = rsqrtf(ss * (1.0f / D) + a.rms_eps);
             if (r < e.n) {
                 const size_t base = ((size_t)(e.t0 + r) * H + h) * D + 32 * part;
-                for (int t = 0; t < 32; t += 2) {
-                    const int jj = 32 * part + t;
-                    float y0 = Ost[r * 129 + jj] * rr * __ldg(a.norm_w + jj);
-                    float y1 = Ost[r * 129 + jj + 1] * rr * __ldg(a.norm_w + jj + 1);
-                    if (a.z) {
-                        const uint32_t zz = *reinterpret_cast<const uint32_t *>(a.z + base + t);
-                        y0 *= sigmoidf_(bf2f((uint16_t)(zz & 0xffff)));
-                        y1 *= sigmoidf_(bf2f((uint16_t)(zz >> 16)));
+                uint4 yo[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t zw[4] = {zr[u].x, zr[u].y, zr[u].z, zr[u].w};
+                    uint32_t yw[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int jj = 32 * part + 8 * u + 2 * q;
+                        float y0 = Ost[r * 129 + jj] * rr * nw[jj];
+                        float y1 = Ost[r * 129 + jj + 1] * rr * nw[jj + 1];
+                        if (a.z) {
+                            y0 *= sigmoidf_(bf2f((uint16_t)(zw[q] & 0xffff)));
+                            y1 *= sigmoidf_(bf2f((uint16_t)(zw[q] >> 16)));
+                        }
+                        yw[q] = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
                     }
-                    *reinterpret_cast<uint32_t *>(a.y + base + t) = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
+                    yo[u] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
                 }
+                uint4 *yp = reinterpret_cast<uint4 *>(a.y + base);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) yp[u] = yo[u];
             }
         }
         // new state: bf16 operand tile for the next chunk; checkpoint when this chunk ends on a boundary

@@ -269,3 +269,19 @@ def test_prefill_full_size_sampled_heads():
     heads = [0, 21]
     ref = p.reference(heads)
     p.check(ref, heads)
+
+
+def test_prefill_wide_decay_range_and_large_values():
+    """Decay logits near -8 (alpha ~ 3e-4) on runs of consecutive tokens in some channels, and values
+    scaled by 50: the chunk's cumulative log-decay spans far more than the range one reference point
+    can carry in fp32, so the intra-chunk products take the exact pairwise form."""
+    kda = _kda()
+    p = Problem(kda, 2, 128, 128, [200, 90], [0, 37], [-1, 3], [0, 3], 64, 128, 16, seed=13)
+    a = ki.bf16_bits_to_f32(p.tok["a"]).copy()
+    a[10:70, :, :16] = -8.0                  # channels 0..15 decay almost fully for 60 tokens
+    a[150:160, 1, 40:60] = -6.0
+    p.tok["a"] = ki.f32_to_bf16_bits(a)
+    v = ki.bf16_bits_to_f32(p.tok["v"]) * 50.0
+    p.tok["v"] = ki.f32_to_bf16_bits(v)
+    assert p.run() == 0
+    p.check(p.reference())
