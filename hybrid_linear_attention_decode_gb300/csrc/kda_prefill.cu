@@ -518,12 +518,20 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 //   P6     [32K,48K) -W bf16 staging | [64K,96K) U' fp32 staging
 constexpr uint32_t I_Q = 0, I_K = 32768, I_G = 65536, I_VT = 98304, I_RAW = 131072;
 constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_INV = 147456, I_T = 163840;
-constexpr uint32_t I_MISC = 184320;   // beta[64], exp(G_mid)[128], exp(G_last)[128], barrier, tensor-memory address
-constexpr uint32_t I_SMEM = I_MISC + 2048 + 1024;  // + alignment slack
+constexpr uint32_t I_MISC = 184320;   // beta[64], exp(G_mid)[128], decay partial sums[4][128], barrier, tmem address
+constexpr uint32_t I_SMEM = I_MISC + 4096 + 1024;  // + alignment slack
 constexpr int RAW_ROWS = CH + kConvW - 1;           // 3 history rows + 64 tokens
 static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
 
-__global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillArgs a, const Layout2 L) {
+constexpr int NTI = 512;  // intra kernel threads
+
+__device__ __forceinline__ float log_sigmoid_fast(float x) {
+    // log(sigmoid(x)) = min(x, 0) - log(1 + exp(-|x|)); absolute error ~1e-7, which is what the
+    // cumulative decay (a sum of these) needs
+    return fminf(x, 0.f) - __logf(1.f + __expf(-fabsf(x)));
+}
+
+__global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillArgs a, const Layout2 L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, CC = 3 * D;
@@ -543,9 +551,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     uint16_t *raw = reinterpret_cast<uint16_t *>(sm + I_RAW);  // [67][384] bf16, row = position p0 - 3 + row
     float *beta = reinterpret_cast<float *>(sm + I_MISC);
     float *eGm = beta + 64;     // exp(G_mid) per channel
-    float *eGl = eGm + D;       // exp(G_last - G_mid) per channel
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + I_MISC + 1536);
-    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + I_MISC + 1600);
+    float *gtot = eGm + D;      // [4][128] partial sums of the cumulative decay
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + I_MISC + 3072);
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + I_MISC + 3136);
     uint8_t *blk = reinterpret_cast<uint8_t *>(a.ws) + L.off_blk + ((size_t)c * H + h) * WS_BLOCK;
 
     if (warp == 0) umma::alloc(tmem_s, 256);
@@ -554,8 +562,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         fence_mbar_init();
     }
 
-    // ---- P0: the chunk's raw q|k|v rows (and 3 rows of history) into smem; decay logits; beta ----
-    for (int idx = tid; idx < RAW_ROWS * 48; idx += NT) {
+    // ---- P0: the chunk's raw q|k|v rows (and 3 rows of history) into smem; log decay; beta ----
+    for (int idx = tid; idx < RAW_ROWS * 48; idx += NTI) {
         const int row = idx / 48, part = idx - (idx / 48) * 48;  // 48 x 16 bytes per row: q 16, k 16, v 16
         const int64_t p = p0 - (kConvW - 1) + row;
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
@@ -572,7 +580,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         }
         reinterpret_cast<uint4 *>(raw + row * CC)[part] = val;
     }
-    for (int idx = tid; idx < CH * 16; idx += NT) {
+    for (int idx = tid; idx < CH * 16; idx += NTI) {
         const int r = idx >> 4, part = idx & 15;
         float g8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (r < ntok) {
@@ -580,34 +588,50 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                g8[2 * u] = log_sigmoid(bf2f((uint16_t)(w4[u] & 0xffff)));
-                g8[2 * u + 1] = log_sigmoid(bf2f((uint16_t)(w4[u] >> 16)));
+                g8[2 * u] = log_sigmoid_fast(bf2f((uint16_t)(w4[u] & 0xffff)));
+                g8[2 * u + 1] = log_sigmoid_fast(bf2f((uint16_t)(w4[u] >> 16)));
             }
         }
         float4 *gd = reinterpret_cast<float4 *>(G + r * D + part * 8);
         gd[0] = make_float4(g8[0], g8[1], g8[2], g8[3]);
         gd[1] = make_float4(g8[4], g8[5], g8[6], g8[7]);
     }
-    for (int r = tid; r < CH; r += NT) beta[r] = r < ntok ? sigmoidf_(bf2f(a.b[(size_t)(e.t0 + r) * H + h])) : 0.f;
+    if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(a.b[(size_t)(e.t0 + tid) * H + h])) : 0.f;
     __syncthreads();
-    // ---- P1: causal conv + SiLU, token-parallel from smem; v goes straight into its V^T tile ----
-    for (int idx = tid; idx < CH * CC; idx += NT) {
-        const int r = idx / CC, ch = idx - (idx / CC) * CC;
-        float out = 0.f;
-        if (r < ntok) {
-            const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
-            out = w.w * bf2f(raw[(r + 3) * CC + ch]);
-            out = fmaf(w.x, bf2f(raw[r * CC + ch]), out);
-            out = fmaf(w.y, bf2f(raw[(r + 1) * CC + ch]), out);
-            out = fmaf(w.z, bf2f(raw[(r + 2) * CC + ch]), out);
-            if (a.silu) out = out / (1.f + __expf(-out));
+    // ---- P1: causal conv + SiLU, one channel per thread along the chunk (window in registers) ----
+    if (tid < CC) {
+        const int ch = tid;
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
+        float h0 = bf2f(raw[ch]), h1 = bf2f(raw[CC + ch]), h2 = bf2f(raw[2 * CC + ch]);
+        for (int r0 = 0; r0 < CH; r0 += 4) {
+            float vb[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = r0 + u;
+                float out = 0.f;
+                if (r < ntok) {
+                    const float x = bf2f(raw[(r + 3) * CC + ch]);
+                    out = fmaf(w.w, x, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
+                    if (a.silu) out = __fdividef(out, 1.f + __expf(-out));
+                    h0 = h1;
+                    h1 = h2;
+                    h2 = x;
+                }
+                vb[u] = out;
+            }
+            if (ch < D) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) qh[(r0 + u) * D + ch] = vb[u];
+            } else if (ch < 2 * D) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) kh[(r0 + u) * D + ch - D] = vb[u];
+            } else {
+                umma::st_tf32x4(Vt, D, ch - 2 * D, r0, vb[0], vb[1], vb[2], vb[3]);
+            }
         }
-        if (ch < D) qh[r * D + ch] = out;
-        else if (ch < 2 * D) kh[r * D + ch - D] = out;
-        else umma::st_tf32(Vt, D, ch - 2 * D, r, out);
     }
     __syncthreads();
-    for (int r = warp; r < ntok; r += NT / 32) {
+    for (int r = warp; r < ntok; r += NTI / 32) {
         const float nq = warp_dot_array(qh + r * D, qh + r * D, D);
         const float nk = warp_dot_array(kh + r * D, kh + r * D, D);
         const float rq = rsqrtf(nq + a.l2_eps), rk = rsqrtf(nk + a.l2_eps);
@@ -616,12 +640,19 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
             kh[r * D + i] *= rk;
         }
     }
-    if (tid < D) {
+    {   // cumulative log decay along the chunk: 4 threads per channel, 16 tokens each
+        const int ch = tid & 127, qd = tid >> 7;
         float acc = 0.f;
-        for (int r = 0; r < CH; ++r) {
-            acc += G[r * D + tid];
-            G[r * D + tid] = acc;
+        for (int r = 16 * qd; r < 16 * qd + 16; ++r) {
+            acc += G[r * D + ch];
+            G[r * D + ch] = acc;
         }
+        gtot[qd * D + ch] = acc;
+        __syncthreads();
+        float off = 0.f;
+        for (int q2 = 0; q2 < qd; ++q2) off += gtot[q2 * D + ch];
+        if (qd > 0)
+            for (int r = 16 * qd; r < 16 * qd + 16; ++r) G[r * D + ch] += off;
     }
     __syncthreads();
 
@@ -632,30 +663,38 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         const float g0 = G[tid], gm = G[MID * D + tid], gl = G[(CH - 1) * D + tid];
         wide = (g0 - gm > kMidRange) || (gm - gl > kMidRange);
         eGm[tid] = expf(gm);
-        eGl[tid] = expf(gl - gm);
+        reinterpret_cast<float *>(blk + WS_GL)[tid] = expf(gl);
     }
     const bool slow = __syncthreads_or(wide) != 0;
     uint8_t *X1 = sm + I_X1;
     uint8_t *Km = sm + I_KM;
-    for (int idx = tid; idx < CH * D; idx += NT) {
-        const int r = idx >> 7, i = idx & 127;
-        const float g = G[idx];
-        const float k_ = kh[idx], q_ = qh[idx];
-        float eq;  // exp(G)
-        if (!slow) {
-            const float ep = __expf(g - G[MID * D + i]);
-            const float em = __frcp_rn(ep);
-            umma::st_bf16(X1, 128, r, i, k_ * ep);
-            umma::st_bf16(X1, 128, CH + r, i, q_ * ep);
-            umma::st_bf16(Km, CH, r, i, k_ * em);
-            eq = ep * eGm[i];
-        } else {
-            eq = __expf(g);
+    for (int idx = tid; idx < CH * 16; idx += NTI) {
+        const int r = idx >> 4, i0 = (idx & 15) * 8;  // 8 channels per item
+        float xk[8], xq[8], xm[8], xp[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u;
+            const float g = G[r * D + i], k_ = kh[r * D + i], q_ = qh[r * D + i];
+            float eq;
+            if (!slow) {
+                const float gm = G[MID * D + i];
+                const float ep = __expf(g - gm);
+                xk[u] = k_ * ep;
+                xq[u] = q_ * ep;
+                xm[u] = k_ * __expf(gm - g);
+                eq = ep * eGm[i];
+            } else {
+                eq = __expf(g);
+            }
+            xp[u] = a.scale * q_ * eq;
         }
-        *reinterpret_cast<__nv_bfloat16 *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, i)) =
-            __float2bfloat16_rn(a.scale * q_ * eq);
+        if (!slow) {
+            umma::st_bf16x8(X1, 128, r, i0, xk);
+            umma::st_bf16x8(X1, 128, CH + r, i0, xq);
+            umma::st_bf16x8(Km, CH, r, i0, xm);
+        }
+        umma::st_bf16x8(blk + WS_QP, CH, r, i0, xp);
     }
-    if (tid < D) reinterpret_cast<float *>(blk + WS_GL)[tid] = expf(G[(CH - 1) * D + tid]);
     fence_proxy_async_smem();
     umma::fence_before();
     __syncthreads();
@@ -681,28 +720,34 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     // Inv region, which P4 fills only after the copy-out below
     uint8_t *Qks = slow ? sm + I_INV : sm + I_Q;
     if (ok && !slow) {
-        const int quad = warp & 3, half = warp >> 2;     // lanes 32*quad.., columns 32*half..
         float v[32];
-        umma::ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * half, v);
-        const int row = 32 * quad + lane;
+        const int quad = warp & 3, half = (warp >> 2) & 1;  // warps 0-7: lanes 32*quad.., columns 32*half..
+        if (warp < 8) umma::ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * half, v);
         __syncthreads();  // every warp has read D1 and X1 is no longer read: A may overwrite it
-        if (row < CH) {
+        if (warp < 8) {
+            const int row = 32 * quad + lane;
+            if (row < CH) {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                const int s_ = 32 * half + t;
-                A[row * CH + s_] = s_ < row ? v[t] : 0.f;
-            }
-        } else {
-            const int r = row - CH;
+                for (int t = 0; t < 32; t += 4) {
+                    const int s_ = 32 * half + t;
+                    *reinterpret_cast<float4 *>(A + row * CH + s_) =
+                        make_float4(s_ < row ? v[t] : 0.f, s_ + 1 < row ? v[t + 1] : 0.f, s_ + 2 < row ? v[t + 2] : 0.f,
+                                    s_ + 3 < row ? v[t + 3] : 0.f);
+                }
+            } else {
+                const int r = row - CH;
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                const int s_ = 32 * half + t;
-                umma::st_bf16(Qks, CH, r, s_, s_ <= r ? a.scale * v[t] : 0.f);
+                for (int t = 0; t < 32; t += 8) {
+                    float x8[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) x8[u] = (32 * half + t + u <= r) ? a.scale * v[t + u] : 0.f;
+                    umma::st_bf16x8(Qks, CH, r, 32 * half + t, x8);
+                }
             }
         }
     } else if (ok) {
         // decay range too wide for one reference point: exact pairwise exponentials
-        for (int idx = tid; idx < CH * CH; idx += NT) {
+        for (int idx = tid; idx < CH * CH; idx += NTI) {
             const int r = idx / CH, s_ = idx - (idx / CH) * CH;
             float accA = 0.f, accQ = 0.f;
             if (s_ <= r && r < ntok) {
@@ -724,7 +769,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     {
         const uint4 *s4 = reinterpret_cast<const uint4 *>(Qks);
         uint4 *d4 = reinterpret_cast<uint4 *>(blk + WS_QK);
-        for (int idx = tid; idx < CH * CH * 2 / 16; idx += NT) d4[idx] = s4[idx];
+        for (int idx = tid; idx < CH * CH * 2 / 16; idx += NTI) d4[idx] = s4[idx];
     }
     __syncthreads();
     // ---- P4: T = (I + diag(beta) A)^{-1} diag(beta), blocked by 16 ----
@@ -743,7 +788,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
 #pragma unroll
         for (int r = 0; r < 16; ++r) Inv[(base + r) * CH + base + col] = x[r];
     }
-    for (int idx = tid; idx < CH * CH; idx += NT) {
+    for (int idx = tid; idx < CH * CH; idx += NTI) {
         const int r = idx / CH, s_ = idx - (idx / CH) * CH;
         if ((s_ >> 4) > (r >> 4)) Inv[idx] = 0.f;
     }
@@ -751,7 +796,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     float *P = reinterpret_cast<float *>(sm + I_T);  // [3][16][16] temporaries (K- is dead)
     for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;  // blocks (i, i-d) for i = d..3
-        for (int idx = tid; idx < nb * 256; idx += NT) {  // P_i = sum_{k=i-d}^{i-1} L_ik Inv_k,(i-d)
+        for (int idx = tid; idx < nb * 256; idx += NTI) {  // P_i = sum_{k=i-d}^{i-1} L_ik Inv_k,(i-d)
             const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
             const int i = bi + d, j = i - d;
             const float br = beta[16 * i + rr];
@@ -763,7 +808,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
             P[idx] = acc;
         }
         __syncthreads();
-        for (int idx = tid; idx < nb * 256; idx += NT) {  // Inv_ij = -Inv_ii P_i
+        for (int idx = tid; idx < nb * 256; idx += NTI) {  // Inv_ij = -Inv_ii P_i
             const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
             const int i = bi + d, j = i - d;
             float acc = 0.f;
@@ -774,20 +819,27 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
         __syncthreads();
     }
     uint8_t *Tt = sm + I_T;  // T tf32 [64 r][64 s]: the B operand of W^T = K+^T T^T (K-major: row r, K = s)
-    for (int idx = tid; idx < CH * CH; idx += NT) {
-        const int r = idx / CH, s_ = idx - (idx / CH) * CH;
-        umma::st_tf32(Tt, CH, r, s_, Inv[idx] * beta[s_]);
+    for (int idx = tid; idx < CH * 16; idx += NTI) {
+        const int r = idx >> 4, s0 = (idx & 15) * 4;
+        const float4 iv = *reinterpret_cast<const float4 *>(Inv + r * CH + s0);
+        umma::st_tf32x4(Tt, CH, r, s0, iv.x * beta[s0], iv.y * beta[s0 + 1], iv.z * beta[s0 + 2], iv.w * beta[s0 + 3]);
     }
     __syncthreads();  // A / Inv are dead: Ktil^T may be staged over them
-    // ---- P5: (k exp G)^T tile (A operand) and the Ktil^T workspace tile ----
+    // ---- P5: (k exp G)^T tile (A operand) and the Ktil^T workspace tile, 4 tokens per item ----
     uint8_t *Kpt = sm + I_Q;
     uint8_t *Kts = sm + I_A;
-    for (int idx = tid; idx < CH * D; idx += NT) {
-        const int r = idx >> 7, i = idx & 127;
-        const float g = G[idx], k_ = kh[idx];
-        const float eq = __expf(g);
-        umma::st_tf32(Kpt, D, i, r, k_ * eq);
-        umma::st_tf32(Kts, D, i, r, slow ? k_ * __expf(G[(CH - 1) * D + i] - g) : k_ * eGl[i] * __frcp_rn(__expf(g - G[MID * D + i])));
+    for (int idx = tid; idx < D * 16; idx += NTI) {
+        const int i = idx & 127, r0 = (idx >> 7) * 4;
+        const float glast = G[(CH - 1) * D + i];
+        float kp[4], kt[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float g = G[(r0 + u) * D + i], k_ = kh[(r0 + u) * D + i];
+            kp[u] = k_ * __expf(g);
+            kt[u] = k_ * __expf(glast - g);
+        }
+        umma::st_tf32x4(Kpt, D, i, r0, kp[0], kp[1], kp[2], kp[3]);
+        umma::st_tf32x4(Kts, D, i, r0, kt[0], kt[1], kt[2], kt[3]);
     }
     fence_proxy_async_smem();
     umma::fence_before();
@@ -805,7 +857,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     {
         const uint4 *s4 = reinterpret_cast<const uint4 *>(Kts);
         uint4 *d4 = reinterpret_cast<uint4 *>(blk + WS_KT);
-        for (int idx = tid; idx < D * CH * 4 / 16; idx += NT) d4[idx] = s4[idx];
+        for (int idx = tid; idx < D * CH * 4 / 16; idx += NTI) d4[idx] = s4[idx];
     }
     ok = wait_all(bar, phase);
     phase ^= 1;
@@ -818,7 +870,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     // ---- P6: -W (bf16 tile [64 r][128 i]) and U' (fp32 [64 r][128 j]) via smem staging ----
     uint8_t *Wst = sm + I_K;
     float *Ust = reinterpret_cast<float *>(sm + I_G);
-    {
+    if (warp < 8) {
         const int quad = warp & 3, half = warp >> 2;
         const int row = 32 * quad + lane;  // channel i (for W^T) / j (for U'^T)
         float v[32];
@@ -834,10 +886,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     {
         const uint4 *s1 = reinterpret_cast<const uint4 *>(Wst);
         uint4 *d1 = reinterpret_cast<uint4 *>(blk + WS_W);
-        for (int idx = tid; idx < CH * D * 2 / 16; idx += NT) d1[idx] = s1[idx];
+        for (int idx = tid; idx < CH * D * 2 / 16; idx += NTI) d1[idx] = s1[idx];
         const uint4 *s2 = reinterpret_cast<const uint4 *>(Ust);
         uint4 *d2 = reinterpret_cast<uint4 *>(blk + WS_UP);
-        for (int idx = tid; idx < CH * D * 4 / 16; idx += NT) d2[idx] = s2[idx];
+        for (int idx = tid; idx < CH * D * 4 / 16; idx += NTI) d2[idx] = s2[idx];
     }
     if (warp == 0) umma::dealloc(tmem, 256);
 
@@ -858,7 +910,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_intra_tc_kernel(const PrefillAr
     for (int w = 0; w < 2; ++w) {
         if (wslot[w] < 0) continue;
         uint16_t *cw = a.conv + ((size_t)wslot[w] * H + h) * (kConvW - 1) * CC;
-        for (int idx = tid; idx < (kConvW - 1) * CC; idx += NT) {
+        for (int idx = tid; idx < (kConvW - 1) * CC; idx += NTI) {
             const int row = idx / CC, ch = idx - (idx / CC) * CC;
             cw[idx] = raw_at(a, D, D, h, ch, pend - (kConvW - 1) + row, start, ts, srcv);
         }
@@ -937,13 +989,20 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
                 v[t] = src >= 0 ? a.S[(((size_t)src * H + h) * D + i0 + t) * D + j] : 0.f;
             umma::st32(tmem + lane_off + T_S + i0, v);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) umma::st_bf16(Sst, D, j, i0 + t, v[t]);
+            for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
         }
     }
     uint32_t ph_ops = 0, ph_mma = 0;
     bool ok = true;
     for (int32_t c = c0; c < c1 && ok; ++c) {
         const ChunkEnt e = ent[c];
+        const int64_t pend = pos[c] + e.n;
+        int ck = -1;  // checkpoint slot of this chunk's end (looked up early; used after the state update)
+        if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
+            const int64_t jj = pend / a.interval - start / a.interval - 1;
+            const int s_ = a.ckpt_slots[a.ckpt_offsets[n] + jj];
+            if (s_ >= 0 && s_ < a.num_slots) ck = s_;
+        }
         // this thread's slice of the output gate, fetched early: token tid/4, channels 32*(tid%4)..
         uint4 zr[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
                        make_uint4(0u, 0u, 0u, 0u)};
@@ -985,10 +1044,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
             float v[32];
             umma::ld32(tmem + lane_off + T_U + 32 * half, v);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                umma::st_tf32(Ut32, D, j, 32 * half + t, v[t]);
-                umma::st_bf16(Ut16, D, j, 32 * half + t, v[t]);
-            }
+            for (int t = 0; t < 32; t += 4) umma::st_tf32x4(Ut32, D, j, 32 * half + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
+#pragma unroll
+            for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Ut16, D, j, 32 * half + t, v + t);
             const float *gl = reinterpret_cast<const float *>(ops + WS_GL);
             for (int part = 0; part < 2; ++part) {
                 const int i0 = 64 * half + 32 * part;
@@ -1066,20 +1124,13 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
             }
         }
         // new state: bf16 operand tile for the next chunk; checkpoint when this chunk ends on a boundary
-        const int64_t pend = pos[c] + e.n;
-        int ck = -1;
-        if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
-            const int64_t jj = pend / a.interval - start / a.interval - 1;
-            const int s = a.ckpt_slots[a.ckpt_offsets[n] + jj];
-            if (s >= 0 && s < a.num_slots) ck = s;
-        }
         {
             float v[32];
             for (int part = 0; part < 2; ++part) {
                 const int i0 = 64 * half + 32 * part;
                 umma::ld32(tmem + lane_off + T_S + i0, v);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) umma::st_bf16(Sst, D, j, i0 + t, v[t]);
+                for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
                 if (ck >= 0) {
 #pragma unroll
                     for (int t = 0; t < 32; ++t) a.S[(((size_t)ck * H + h) * D + i0 + t) * D + j] = v[t];
@@ -1142,7 +1193,7 @@ static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     prefill_table_kernel<<<1, kMaxSeqThreads, 0, st>>>(a, tc::as_layout(L2));
     if (a.total_tokens > 0) {
         dim3 gi((unsigned)L2.maxc, a.H);
-        tc::prefill_intra_tc_kernel<<<gi, tc::NT, tc::I_SMEM, st>>>(a, L2);
+        tc::prefill_intra_tc_kernel<<<gi, tc::NTI, tc::I_SMEM, st>>>(a, L2);
     }
     dim3 gs(a.nseq, a.H);
     tc::prefill_state_tc_kernel<<<gs, tc::NT, tc::S_SMEM, st>>>(a, L2);

@@ -41,6 +41,23 @@ __device__ __forceinline__ void st_bf16(uint8_t *tile, int R, int r, int k, floa
     *reinterpret_cast<__nv_bfloat16 *>(tile + sw128_offset<2>(R, r, k)) = __float2bfloat16_rn(x);
 }
 
+// 16-byte stores of 4 consecutive tf32 (k0 % 4 == 0) / 8 consecutive bf16 (k0 % 8 == 0) elements of a row.
+__device__ __forceinline__ void st_tf32x4(uint8_t *tile, int R, int r, int k0, float x0, float x1, float x2,
+                                          float x3) {
+    *reinterpret_cast<uint4 *>(tile + sw128_offset<4>(R, r, k0)) = make_uint4(to_tf32(x0), to_tf32(x1), to_tf32(x2),
+                                                                              to_tf32(x3));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+__device__ __forceinline__ void st_bf16x8(uint8_t *tile, int R, int r, int k0, const float *x) {
+    *reinterpret_cast<uint4 *>(tile + sw128_offset<2>(R, r, k0)) =
+        make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
+
 // Shared-memory matrix descriptor: start address, leading / stride byte offsets, 128B swizzle.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
     uint64_t d = 0;
