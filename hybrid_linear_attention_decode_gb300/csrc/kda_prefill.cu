@@ -513,14 +513,19 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 // Intra-chunk kernel smem (bytes, from a 1024-aligned base), by phase:
 //   P0-P1  [0,32K) q^ fp32 | [32K,64K) k^ fp32 | [64K,96K) G fp32 | [96K,128K) V^T tf32 tile | [128K,180K) raw rows
 //   P2     [128K,160K) [K+;Q+] bf16 tile | [160K,176K) K- bf16 tile
-//   P3-P4  [0,8K) Qk staging | [128K,144K) A fp32 | [144K,160K) Inv fp32 | [160K,176K) block temps, then T tf32
+//   P3-P4  [0,8K) Qk staging, then [0,16K) Inv fp32 | [128K,145K) A fp32 (row stride 68) | [160K,176K) block temps,
+//          then T tf32
 //   P5     [0,32K) (k exp G)^T tf32 tile | [128K,160K) Ktil^T tf32 staging
 //   P6     [32K,48K) -W bf16 staging | [64K,96K) U' fp32 staging
 constexpr uint32_t I_Q = 0, I_K = 32768, I_G = 65536, I_VT = 98304, I_RAW = 131072;
-constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_INV = 147456, I_T = 163840;
-constexpr uint32_t I_MISC = 184320;   // beta[64], exp(G_mid)[128], decay partial sums[4][128], barrier, tmem address
-constexpr uint32_t I_SMEM = I_MISC + 4096 + 1024;  // + alignment slack
+constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_T = 163840;
+constexpr uint32_t I_INV = 0;          // Inv fp32 [64][64] over q^ (free after the Qk copy-out)
+constexpr uint32_t I_QKS_SLOW = 148480; // Qk staging of the wide-decay path (q^ is still read there)
+constexpr uint32_t I_MISC = 184320;   // beta, exp(G_mid), decay partial sums, barrier, tmem address, window stash
+constexpr uint32_t I_SMEM = I_MISC + 6144 + 1024;  // + alignment slack
 constexpr int RAW_ROWS = CH + kConvW - 1;           // 3 history rows + 64 tokens
+constexpr int AST = 68;                             // row stride of A in smem (padded against bank conflicts)
+static_assert(I_A + CH * AST * 4 <= I_QKS_SLOW && I_QKS_SLOW + CH * CH * 2 <= I_T, "A and slow Qk staging");
 static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
 
 constexpr int NTI = 512;  // intra kernel threads
@@ -563,38 +568,54 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
     }
 
     // ---- P0: the chunk's raw q|k|v rows (and 3 rows of history) into smem; log decay; beta ----
-    for (int idx = tid; idx < RAW_ROWS * 48; idx += NTI) {
-        const int row = idx / 48, part = idx - (idx / 48) * 48;  // 48 x 16 bytes per row: q 16, k 16, v 16
-        const int64_t p = p0 - (kConvW - 1) + row;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (row < (kConvW - 1) + ntok) {
-            if (p >= start) {
-                const size_t t = (size_t)(ts + (p - start)) * H + h;
-                const uint16_t *srcp = part < 16 ? a.q + t * D : (part < 32 ? a.k + t * D : a.v + t * D);
-                val = __ldg(reinterpret_cast<const uint4 *>(srcp) + (part & 15));
-            } else if (srcv >= 0) {
-                const int crow = (int)(p - start + (kConvW - 1));
-                val = __ldg(reinterpret_cast<const uint4 *>(a.conv + (((size_t)srcv * H + h) * (kConvW - 1) + crow) * CC) +
-                            part);
-            }
-        }
-        reinterpret_cast<uint4 *>(raw + row * CC)[part] = val;
-    }
-    for (int idx = tid; idx < CH * 16; idx += NTI) {
-        const int r = idx >> 4, part = idx & 15;
-        float g8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (r < ntok) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.a + ((size_t)(e.t0 + r) * H + h) * D) + part);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    // Every load of a thread is issued before its first store, so the loads are in flight together.
+    constexpr int RAW_IT = (RAW_ROWS * 48 + NTI - 1) / NTI;
+    {
+        uint4 val[RAW_IT];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                g8[2 * u] = log_sigmoid_fast(bf2f((uint16_t)(w4[u] & 0xffff)));
-                g8[2 * u + 1] = log_sigmoid_fast(bf2f((uint16_t)(w4[u] >> 16)));
+        for (int u = 0; u < RAW_IT; ++u) {
+            const int idx = tid + u * NTI;
+            val[u] = make_uint4(0u, 0u, 0u, 0u);
+            const int row = idx / 48, part = idx - (idx / 48) * 48;  // 48 x 16 bytes per row: q, k, v
+            const int64_t p = p0 - (kConvW - 1) + row;
+            if (idx < RAW_ROWS * 48 && row < (kConvW - 1) + ntok) {
+                if (p >= start) {
+                    const size_t t = (size_t)(ts + (p - start)) * H + h;
+                    const uint16_t *srcp = part < 16 ? a.q + t * D : (part < 32 ? a.k + t * D : a.v + t * D);
+                    val[u] = __ldg(reinterpret_cast<const uint4 *>(srcp) + (part & 15));
+                } else if (srcv >= 0) {
+                    const int crow = (int)(p - start + (kConvW - 1));
+                    val[u] = __ldg(reinterpret_cast<const uint4 *>(
+                                       a.conv + (((size_t)srcv * H + h) * (kConvW - 1) + crow) * CC) + part);
+                }
             }
         }
-        float4 *gd = reinterpret_cast<float4 *>(G + r * D + part * 8);
-        gd[0] = make_float4(g8[0], g8[1], g8[2], g8[3]);
-        gd[1] = make_float4(g8[4], g8[5], g8[6], g8[7]);
+        uint4 av[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int idx = tid + u * NTI, r = idx >> 4, part = idx & 15;
+            av[u] = r < ntok ? __ldg(reinterpret_cast<const uint4 *>(a.a + ((size_t)(e.t0 + r) * H + h) * D) + part)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < RAW_IT; ++u) {
+            const int idx = tid + u * NTI;
+            if (idx < RAW_ROWS * 48) reinterpret_cast<uint4 *>(raw)[idx] = val[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int idx = tid + u * NTI, r = idx >> 4, part = idx & 15;
+            const uint32_t w4[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
+            float g8[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                g8[2 * q] = r < ntok ? log_sigmoid_fast(bf2f((uint16_t)(w4[q] & 0xffff))) : 0.f;
+                g8[2 * q + 1] = r < ntok ? log_sigmoid_fast(bf2f((uint16_t)(w4[q] >> 16))) : 0.f;
+            }
+            float4 *gd = reinterpret_cast<float4 *>(G + r * D + part * 8);
+            gd[0] = make_float4(g8[0], g8[1], g8[2], g8[3]);
+            gd[1] = make_float4(g8[4], g8[5], g8[6], g8[7]);
+        }
     }
     if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(a.b[(size_t)(e.t0 + tid) * H + h])) : 0.f;
     __syncthreads();
@@ -603,34 +624,36 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
         const int ch = tid;
         const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
         float h0 = bf2f(raw[ch]), h1 = bf2f(raw[CC + ch]), h2 = bf2f(raw[2 * CC + ch]);
-        for (int r0 = 0; r0 < CH; r0 += 4) {
-            float vb[4];
+        for (int r0 = 0; r0 < CH; r0 += 8) {
+            float xs8[8], ob[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int r = r0 + u;
-                float out = 0.f;
-                if (r < ntok) {
-                    const float x = bf2f(raw[(r + 3) * CC + ch]);
-                    out = fmaf(w.w, x, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
-                    if (a.silu) out = __fdividef(out, 1.f + __expf(-out));
-                    h0 = h1;
-                    h1 = h2;
-                    h2 = x;
-                }
-                vb[u] = out;
+            for (int u = 0; u < 8; ++u) xs8[u] = bf2f(raw[(r0 + u + 3) * CC + ch]);  // all taps before any store
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float x = xs8[u];
+                float out = fmaf(w.w, x, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
+                if (a.silu) out = __fdividef(out, 1.f + __expf(-out));
+                ob[u] = (r0 + u < ntok) ? out : 0.f;
+                h0 = h1;
+                h1 = h2;
+                h2 = x;
             }
             if (ch < D) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) qh[(r0 + u) * D + ch] = vb[u];
+                for (int u = 0; u < 8; ++u) qh[(r0 + u) * D + ch] = ob[u];
             } else if (ch < 2 * D) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) kh[(r0 + u) * D + ch - D] = vb[u];
+                for (int u = 0; u < 8; ++u) kh[(r0 + u) * D + ch - D] = ob[u];
             } else {
-                umma::st_tf32x4(Vt, D, ch - 2 * D, r0, vb[0], vb[1], vb[2], vb[3]);
+                umma::st_tf32x4(Vt, D, ch - 2 * D, r0, ob[0], ob[1], ob[2], ob[3]);
+                umma::st_tf32x4(Vt, D, ch - 2 * D, r0 + 4, ob[4], ob[5], ob[6], ob[7]);
             }
         }
     }
     __syncthreads();
+    // raw rows of positions pend-3 .. pend-1 (the conv window after this chunk), kept past P2
+    uint4 *wstash = reinterpret_cast<uint4 *>(sm + I_MISC + 3200);
+    if (tid < 3 * CC / 8) wstash[tid] = reinterpret_cast<const uint4 *>(raw + ntok * CC)[tid];
     for (int r = warp; r < ntok; r += NTI / 32) {
         const float nq = warp_dot_array(qh + r * D, qh + r * D, D);
         const float nk = warp_dot_array(kh + r * D, kh + r * D, D);
@@ -670,19 +693,27 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
     uint8_t *Km = sm + I_KM;
     for (int idx = tid; idx < CH * 16; idx += NTI) {
         const int r = idx >> 4, i0 = (idx & 15) * 8;  // 8 channels per item
-        float xk[8], xq[8], xm[8], xp[8];
+        float xk[8], xq[8], xm[8], xp[8], gv[8], kv[8], qv[8], gmv[8], egv[8];
+        *reinterpret_cast<float4 *>(gv) = *reinterpret_cast<const float4 *>(G + r * D + i0);
+        *reinterpret_cast<float4 *>(gv + 4) = *reinterpret_cast<const float4 *>(G + r * D + i0 + 4);
+        *reinterpret_cast<float4 *>(kv) = *reinterpret_cast<const float4 *>(kh + r * D + i0);
+        *reinterpret_cast<float4 *>(kv + 4) = *reinterpret_cast<const float4 *>(kh + r * D + i0 + 4);
+        *reinterpret_cast<float4 *>(qv) = *reinterpret_cast<const float4 *>(qh + r * D + i0);
+        *reinterpret_cast<float4 *>(qv + 4) = *reinterpret_cast<const float4 *>(qh + r * D + i0 + 4);
+        *reinterpret_cast<float4 *>(gmv) = *reinterpret_cast<const float4 *>(G + MID * D + i0);
+        *reinterpret_cast<float4 *>(gmv + 4) = *reinterpret_cast<const float4 *>(G + MID * D + i0 + 4);
+        *reinterpret_cast<float4 *>(egv) = *reinterpret_cast<const float4 *>(eGm + i0);
+        *reinterpret_cast<float4 *>(egv + 4) = *reinterpret_cast<const float4 *>(eGm + i0 + 4);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u;
-            const float g = G[r * D + i], k_ = kh[r * D + i], q_ = qh[r * D + i];
+            const float g = gv[u], k_ = kv[u], q_ = qv[u];
             float eq;
             if (!slow) {
-                const float gm = G[MID * D + i];
-                const float ep = __expf(g - gm);
+                const float ep = __expf(g - gmv[u]);
                 xk[u] = k_ * ep;
                 xq[u] = q_ * ep;
-                xm[u] = k_ * __expf(gm - g);
-                eq = ep * eGm[i];
+                xm[u] = k_ * __expf(gmv[u] - g);
+                eq = ep * egv[u];
             } else {
                 eq = __expf(g);
             }
@@ -714,11 +745,10 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
         umma::fence_after();
     }
     // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with diagonal, bf16 tile) ----
-    float *A = reinterpret_cast<float *>(sm + I_A);      // [64][64]
+    float *A = reinterpret_cast<float *>(sm + I_A);      // [64][AST]
     float *Inv = reinterpret_cast<float *>(sm + I_INV);  // [64][64]
-    // Qk tile staging: over q^ (dead) on the fast path; the slow path still reads q^, so it stages in the
-    // Inv region, which P4 fills only after the copy-out below
-    uint8_t *Qks = slow ? sm + I_INV : sm + I_Q;
+    // Qk tile staging: over q^ (dead) on the fast path; the slow path still reads q^, so it stages behind A
+    uint8_t *Qks = slow ? sm + I_QKS_SLOW : sm + I_Q;
     if (ok && !slow) {
         float v[32];
         const int quad = warp & 3, half = (warp >> 2) & 1;  // warps 0-7: lanes 32*quad.., columns 32*half..
@@ -730,7 +760,7 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
 #pragma unroll
                 for (int t = 0; t < 32; t += 4) {
                     const int s_ = 32 * half + t;
-                    *reinterpret_cast<float4 *>(A + row * CH + s_) =
+                    *reinterpret_cast<float4 *>(A + row * AST + s_) =
                         make_float4(s_ < row ? v[t] : 0.f, s_ + 1 < row ? v[t + 1] : 0.f, s_ + 2 < row ? v[t + 2] : 0.f,
                                     s_ + 3 < row ? v[t + 3] : 0.f);
                 }
@@ -757,7 +787,7 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
                     accQ = fmaf(qh[r * D + i], ks, accQ);
                 }
             }
-            A[idx] = s_ < r ? accA : 0.f;
+            A[r * AST + s_] = s_ < r ? accA : 0.f;
             umma::st_bf16(Qks, CH, r, s_, s_ <= r ? a.scale * accQ : 0.f);
         }
     }
@@ -782,7 +812,7 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
             float acc = (r == col) ? 1.f : 0.f;
             const float br = beta[base + r];
 #pragma unroll
-            for (int s_ = 0; s_ < r; ++s_) acc = fmaf(-br * A[(base + r) * CH + base + s_], x[s_], acc);
+            for (int s_ = 0; s_ < r; ++s_) acc = fmaf(-br * A[(base + r) * AST + base + s_], x[s_], acc);
             x[r] = acc;
         }
 #pragma unroll
@@ -799,13 +829,12 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
         for (int idx = tid; idx < nb * 256; idx += NTI) {  // P_i = sum_{k=i-d}^{i-1} L_ik Inv_k,(i-d)
             const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
             const int i = bi + d, j = i - d;
-            const float br = beta[16 * i + rr];
             float acc = 0.f;
             for (int k = j; k < i; ++k)
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
-                    acc = fmaf(br * A[(16 * i + rr) * CH + 16 * k + t], Inv[(16 * k + t) * CH + 16 * j + cc], acc);
-            P[idx] = acc;
+                    acc = fmaf(A[(16 * i + rr) * AST + 16 * k + t], Inv[(16 * k + t) * CH + 16 * j + cc], acc);
+            P[idx] = beta[16 * i + rr] * acc;
         }
         __syncthreads();
         for (int idx = tid; idx < nb * 256; idx += NTI) {  // Inv_ij = -Inv_ii P_i
@@ -909,11 +938,8 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
     if (pend == start + len) wslot[1] = a.dst[n];
     for (int w = 0; w < 2; ++w) {
         if (wslot[w] < 0) continue;
-        uint16_t *cw = a.conv + ((size_t)wslot[w] * H + h) * (kConvW - 1) * CC;
-        for (int idx = tid; idx < (kConvW - 1) * CC; idx += NTI) {
-            const int row = idx / CC, ch = idx - (idx / CC) * CC;
-            cw[idx] = raw_at(a, D, D, h, ch, pend - (kConvW - 1) + row, start, ts, srcv);
-        }
+        uint4 *cw = reinterpret_cast<uint4 *>(a.conv + ((size_t)wslot[w] * H + h) * (kConvW - 1) * CC);
+        if (tid < 3 * CC / 8) cw[tid] = wstash[tid];
     }
 }
 
