@@ -567,55 +567,71 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
         fence_mbar_init();
     }
 
-    // ---- P0: the chunk's raw q|k|v rows (and 3 rows of history) into smem; log decay; beta ----
-    // Every load of a thread is issued before its first store, so the loads are in flight together.
-    constexpr int RAW_IT = (RAW_ROWS * 48 + NTI - 1) / NTI;
-    {
-        uint4 val[RAW_IT];
-#pragma unroll
-        for (int u = 0; u < RAW_IT; ++u) {
-            const int idx = tid + u * NTI;
-            val[u] = make_uint4(0u, 0u, 0u, 0u);
-            const int row = idx / 48, part = idx - (idx / 48) * 48;  // 48 x 16 bytes per row: q, k, v
-            const int64_t p = p0 - (kConvW - 1) + row;
-            if (idx < RAW_ROWS * 48 && row < (kConvW - 1) + ntok) {
-                if (p >= start) {
-                    const size_t t = (size_t)(ts + (p - start)) * H + h;
-                    const uint16_t *srcp = part < 16 ? a.q + t * D : (part < 32 ? a.k + t * D : a.v + t * D);
-                    val[u] = __ldg(reinterpret_cast<const uint4 *>(srcp) + (part & 15));
-                } else if (srcv >= 0) {
-                    const int crow = (int)(p - start + (kConvW - 1));
-                    val[u] = __ldg(reinterpret_cast<const uint4 *>(
-                                       a.conv + (((size_t)srcv * H + h) * (kConvW - 1) + crow) * CC) + part);
-                }
+    // ---- P0: the chunk's raw q|k|v rows (and 3 rows of history) and decay logits into smem ----
+    // One 256-byte bulk copy per (row, tensor), issued by one thread each; rows without a source are
+    // zero-filled with ordinary stores.  Row `row` holds position p0 - 3 + row; history rows before the
+    // sequence start come from the source slot's stored window.
+    uint16_t *astage = reinterpret_cast<uint16_t *>(sm + I_VT);  // decay logits bf16 [64][128] (V^T comes later)
+    uint64_t *bar_in = bar + 1;
+    const int nrows = (kConvW - 1) + ntok;                        // rows with data
+    const int hist_src = (int)min((int64_t)nrows, max((int64_t)0, start - p0 + (kConvW - 1)));  // rows before start
+    if (tid == 0) {
+        mbar_init(bar_in, 1);
+        fence_mbar_init();
+        const uint32_t bytes = (uint32_t)((nrows - (srcv >= 0 ? 0 : hist_src)) * 3 * 256 + ntok * 256);
+        mbar_arrive_expect_tx(bar_in, bytes);
+    }
+    __syncthreads();
+    if (tid < RAW_ROWS * 3) {
+        const int row = tid / 3, part = tid - (tid / 3) * 3;
+        const int64_t p = p0 - (kConvW - 1) + row;
+        uint16_t *dst = raw + row * CC + part * D;
+        const uint16_t *src = nullptr;
+        if (row < nrows) {
+            if (p >= start) {
+                const size_t t = (size_t)(ts + (p - start)) * H + h;
+                src = (part == 0 ? a.q : (part == 1 ? a.k : a.v)) + t * D;
+            } else if (srcv >= 0) {
+                src = a.conv + (((size_t)srcv * H + h) * (kConvW - 1) + (p - start + (kConvW - 1))) * CC + part * D;
             }
         }
-        uint4 av[2];
+        if (src) {
+            bulk_g2s(dst, src, 256, bar_in);
+        } else {
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int idx = tid + u * NTI, r = idx >> 4, part = idx & 15;
-            av[u] = r < ntok ? __ldg(reinterpret_cast<const uint4 *>(a.a + ((size_t)(e.t0 + r) * H + h) * D) + part)
-                             : make_uint4(0u, 0u, 0u, 0u);
+            for (int u = 0; u < 16; ++u) d4[u] = make_uint4(0u, 0u, 0u, 0u);
         }
+    } else if (tid >= 256 && tid < 256 + CH) {
+        const int r = tid - 256;
+        uint16_t *dst = astage + r * D;
+        if (r < ntok) {
+            bulk_g2s(dst, a.a + ((size_t)(e.t0 + r) * H + h) * D, 256, bar_in);
+        } else {
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-        for (int u = 0; u < RAW_IT; ++u) {
-            const int idx = tid + u * NTI;
-            if (idx < RAW_ROWS * 48) reinterpret_cast<uint4 *>(raw)[idx] = val[u];
+            for (int u = 0; u < 16; ++u) d4[u] = make_uint4(0u, 0u, 0u, 0u);
         }
+    }
+    if (__syncthreads_or(!mbar_wait(bar_in, 0))) {
+        if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+        __syncthreads();
+        if (warp == 0) umma::dealloc(*tmem_s, 256);
+        return;
+    }
+    for (int idx = tid; idx < CH * 16; idx += NTI) {  // log decay, 8 channels per item
+        const int r = idx >> 4, part = idx & 15;
+        const uint4 v = reinterpret_cast<const uint4 *>(astage + r * D)[part];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        float g8[8];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int idx = tid + u * NTI, r = idx >> 4, part = idx & 15;
-            const uint32_t w4[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
-            float g8[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                g8[2 * q] = r < ntok ? log_sigmoid_fast(bf2f((uint16_t)(w4[q] & 0xffff))) : 0.f;
-                g8[2 * q + 1] = r < ntok ? log_sigmoid_fast(bf2f((uint16_t)(w4[q] >> 16))) : 0.f;
-            }
-            float4 *gd = reinterpret_cast<float4 *>(G + r * D + part * 8);
-            gd[0] = make_float4(g8[0], g8[1], g8[2], g8[3]);
-            gd[1] = make_float4(g8[4], g8[5], g8[6], g8[7]);
+        for (int q = 0; q < 4; ++q) {
+            g8[2 * q] = r < ntok ? log_sigmoid_fast(bf2f((uint16_t)(w4[q] & 0xffff))) : 0.f;
+            g8[2 * q + 1] = r < ntok ? log_sigmoid_fast(bf2f((uint16_t)(w4[q] >> 16))) : 0.f;
         }
+        float4 *gd = reinterpret_cast<float4 *>(G + r * D + part * 8);
+        gd[0] = make_float4(g8[0], g8[1], g8[2], g8[3]);
+        gd[1] = make_float4(g8[4], g8[5], g8[6], g8[7]);
     }
     if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(a.b[(size_t)(e.t0 + tid) * H + h])) : 0.f;
     __syncthreads();
@@ -796,10 +812,12 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
         if (warp == 0) umma::dealloc(tmem, 256);
         return;
     }
-    {
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(Qks);
-        uint4 *d4 = reinterpret_cast<uint4 *>(blk + WS_QK);
-        for (int idx = tid; idx < CH * CH * 2 / 16; idx += NTI) d4[idx] = s4[idx];
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // Qk tile to the workspace; the staging is reused by P4, so wait until it has been read
+        bulk_s2g(blk + WS_QK, Qks, CH * CH * 2);
+        bulk_commit();
+        bulk_wait_read_all();
     }
     __syncthreads();
     // ---- P4: T = (I + diag(beta) A)^{-1} diag(beta), blocked by 16 ----
@@ -883,16 +901,19 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
         }
         umma::commit(bar);
     }
-    {
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(Kts);
-        uint4 *d4 = reinterpret_cast<uint4 *>(blk + WS_KT);
-        for (int idx = tid; idx < D * CH * 4 / 16; idx += NTI) d4[idx] = s4[idx];
+    if (tid == 0) {  // Ktil^T tile to the workspace (its staging is not reused)
+        bulk_s2g(blk + WS_KT, Kts, D * CH * 4);
+        bulk_commit();
     }
     ok = wait_all(bar, phase);
     phase ^= 1;
     umma::fence_after();
     if (!ok) {
-        if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+        if (tid == 0) {
+            set_status(a.status, KDA_DEV_TIMEOUT);
+            bulk_wait_all();  // the Ktil^T copy still reads this CTA's shared memory
+        }
+        __syncthreads();
         if (warp == 0) umma::dealloc(tmem, 256);
         return;
     }
@@ -910,15 +931,14 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
 #pragma unroll
         for (int t = 0; t < 32; ++t) Ust[(32 * half + t) * D + row] = v[t];
     }
+    fence_proxy_async_smem();
     umma::fence_before();
     __syncthreads();
-    {
-        const uint4 *s1 = reinterpret_cast<const uint4 *>(Wst);
-        uint4 *d1 = reinterpret_cast<uint4 *>(blk + WS_W);
-        for (int idx = tid; idx < CH * D * 2 / 16; idx += NTI) d1[idx] = s1[idx];
-        const uint4 *s2 = reinterpret_cast<const uint4 *>(Ust);
-        uint4 *d2 = reinterpret_cast<uint4 *>(blk + WS_UP);
-        for (int idx = tid; idx < CH * D * 4 / 16; idx += NTI) d2[idx] = s2[idx];
+    if (tid == 0) {  // -W and U' to the workspace; every bulk copy of this CTA completes before it exits
+        bulk_s2g(blk + WS_W, Wst, CH * D * 2);
+        bulk_s2g(blk + WS_UP, Ust, CH * D * 4);
+        bulk_commit();
+        bulk_wait_all();
     }
     if (warp == 0) umma::dealloc(tmem, 256);
 
