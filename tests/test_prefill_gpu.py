@@ -285,3 +285,76 @@ def test_prefill_wide_decay_range_and_large_values():
     p.tok["v"] = ki.f32_to_bf16_bits(v)
     assert p.run() == 0
     p.check(p.reference())
+
+
+def test_prefix_resume_workload_full_size():
+    """The prefix-resume workload at full size: one 32768-token prefix prefilled with checkpoints every 128
+    tokens; 16 requests copy-on-write the checkpoint at 32768 into private slots and prefill 1024
+    distinct tokens each in one varlen call.  Each result equals, bit for bit, a full replay of its
+    33792 tokens; two heads of one request also match the oracle."""
+    kda = _kda()
+    H, D, C, I, P, R, L = 32, 128, 64, 128, 32768, 16, 1024
+    pre = Problem(kda, H, D, D, [P], [0], [-1], [0], C, I, 320, seed=50, fill=False)
+    assert pre.run() == 0
+    shared = int(pre.ck[-1])  # the boundary at 32768
+    assert oracle.ckpt_positions(0, P, I)[-1] == P
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    priv = list(range(300, 300 + R))
+    kda.kda_resume_from_slot(pre.pool, torch.tensor([shared] * R, dtype=torch.int32, device="cuda"),
+                             torch.tensor(priv, dtype=torch.int32, device="cuda"), status)
+    suffix = [ki.token_inputs(500 + r, L, H, D, D) for r in range(R)]
+    res = Problem.__new__(Problem)
+    res.__dict__.update(pre.__dict__)
+    res.lens, res.starts, res.src, res.dst, res.T = [L] * R, [P] * R, priv, priv, R * L
+    res.cu = np.arange(R + 1, dtype=np.int32) * L
+    res.tok = {k: np.concatenate([s[k] for s in suffix]) for k in suffix[0]}
+    res.interval, res.offs, res.ck = 0, np.zeros(R + 1, dtype=np.int32), np.zeros(0, dtype=np.int32)
+    assert res.run() == 0
+    y_res = res.y.clone()
+    for r in (0, 7, 15):  # full replays of three of the requests
+        rep = Problem.__new__(Problem)
+        rep.__dict__.update(pre.__dict__)
+        rep.lens, rep.starts, rep.src, rep.dst, rep.T = [P + L], [0], [-1], [310], P + L
+        rep.cu = np.array([0, P + L], dtype=np.int32)
+        rep.tok = {k: np.concatenate([pre.tok[k], suffix[r][k]]) for k in suffix[0]}
+        rep.interval, rep.offs, rep.ck = 0, np.zeros(2, dtype=np.int32), np.zeros(0, dtype=np.int32)
+        assert rep.run() == 0
+        assert torch.equal(rep.y[P:].view(torch.int16), y_res[r * L:(r + 1) * L].view(torch.int16))
+        assert torch.equal(pre.pool.S[310], pre.pool.S[priv[r]])
+        assert torch.equal(pre.pool.conv[310].view(torch.int16), pre.pool.conv[priv[r]].view(torch.int16))
+        if r == 15:
+            ref = rep.reference(heads=[3, 30])
+            assert y_err(bf16_dev_to_f64(y_res[r * L:(r + 1) * L])[:, [3, 30]], ref["y"][P:]) <= Y_TOL
+            assert s_err(pre.pool.S[priv[r]].cpu().numpy()[[3, 30]], ref["S"][0]) <= S_TOL
+
+
+def test_long_context_workload_full_size():
+    """The long-context workload: one 131072-token prefill (H=32, dk=dv=128, chunk 64, checkpoints every
+    32768 tokens), then a batch-256 decode step in which one request continues this sequence from its
+    final state and 255 use random slots.  Two heads against the oracle at every output, checkpoint,
+    the final state and the decode step."""
+    kda = _kda()
+    H, D, T, I = 32, 128, 131072, 32768
+    p = Problem(kda, H, D, D, [T], [0], [-1], [0], 64, I, 512, seed=60, fill=False)
+    assert p.run() == 0
+    assert len(p.ck) == 4
+    heads = [5, 26]
+    ref = p.reference(heads)
+    p.check(ref, heads)
+    # decode at batch 256: request 0 continues slot 0, the others use random slots (zero states here)
+    N = 256
+    slots = [0] + [int(s) for s in ki.random_slots(61, 512, N + 8)[1:] if int(s) not in p.ck and s != 0][:N - 1]
+    tok = ki.token_inputs(62, N, H, D, D)
+    dev = {k: to_dev_bf16(v) for k, v in tok.items()}
+    y = torch.empty(N, H, D, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sl = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    kda.kda_decode_step(p.pool, p.prm, dev["q"], dev["k"], dev["v"], dev["a"], dev["b"], dev["z"], y, sl, sl, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    cfg = oracle.Cfg(H=len(heads), dk=D, dv=D)
+    f = {k: ki.bf16_bits_to_f64(v)[:1, heads] for k, v in tok.items()}
+    dec = oracle.forward(cfg, [0, 1], [T], f["q"], f["k"], f["v"], f["a"], f["b"], f["z"],
+                         p.wts["conv_w"][heads], p.wts["norm_w"], ref["S"], ref["conv"])
+    assert y_err(bf16_dev_to_f64(y[:1])[:, heads], dec["y"]) <= Y_TOL
+    assert s_err(p.pool.S[0].cpu().numpy()[heads], dec["S"][0]) <= S_TOL
