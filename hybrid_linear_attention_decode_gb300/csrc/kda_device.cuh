@@ -17,6 +17,8 @@ __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(stati
 __device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// Fast-division variant for the output gate, which only scales a bf16 output.
+__device__ __forceinline__ float sigmoid_gate(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

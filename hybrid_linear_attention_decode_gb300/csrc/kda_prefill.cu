@@ -972,12 +972,13 @@ constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand
 constexpr uint32_t S_OPS = 32768;     // one chunk's workspace block (Qk, -W, Q+, Ktil^T, gl, U'), WS_BLOCK bytes
 constexpr uint32_t S_UT32 = 140288;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil
 constexpr uint32_t S_UT16 = 173056;   // U^T bf16 tile [128 j][64 r]: A operand of O^T += U^T Qk^T
-constexpr uint32_t S_OST = 189440;    // O staging fp32 [64 r][129]
-constexpr uint32_t S_NW = 222464;     // RMSNorm weight [128]
-constexpr uint32_t S_MISC = 222976;   // barriers, tensor-memory address
+constexpr uint32_t S_OST = 189440;    // O staging fp32 [64 r][OST] (row stride 132: 16-byte rows, conflict-free)
+constexpr int OST = 132;
+constexpr uint32_t S_NW = 223232;     // RMSNorm weight [128]
+constexpr uint32_t S_MISC = 223744;   // barriers, tensor-memory address
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
 static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0 && S_UT16 % 1024 == 0, "state smem layout");
-static_assert(S_OST + CH * 129 * 4 <= S_NW, "state smem layout");
+static_assert(S_OST + CH * OST * 4 <= S_NW, "state smem layout");
 
 // TMEM columns: S^T [0,128), U^T [128,192), O^T [192,256)
 constexpr uint32_t T_S = 0, T_U = 128, T_O = 192;
@@ -1049,14 +1050,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
             const int s_ = a.ckpt_slots[a.ckpt_offsets[n] + jj];
             if (s_ >= 0 && s_ < a.num_slots) ck = s_;
         }
-        // this thread's slice of the output gate, fetched early: token tid/4, channels 32*(tid%4)..
-        uint4 zr[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
-                       make_uint4(0u, 0u, 0u, 0u)};
-        if (a.z && (tid >> 2) < e.n) {
-            const uint4 *zp = reinterpret_cast<const uint4 *>(a.z + ((size_t)(e.t0 + (tid >> 2)) * H + h) * D +
-                                                              32 * (tid & 3));
+        // the output gate of this warp's tokens (warp + 8k), channels 4*lane .. 4*lane+3, fetched early
+        uint2 zr[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) zr[u] = __ldg(zp + u);
+        for (int k8 = 0; k8 < 8; ++k8) {
+            const int r = warp + 8 * k8;
+            zr[k8] = (a.z && r < e.n)
+                         ? __ldg(reinterpret_cast<const uint2 *>(a.z + ((size_t)(e.t0 + r) * H + h) * D) + lane)
+                         : make_uint2(0u, 0u);
         }
         ok = mbar_wait(bar_ops, ph_ops);
         ph_ops ^= 1;
@@ -1130,43 +1131,31 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
             float v[32];
             umma::ld32(tmem + lane_off + T_O + 32 * half, v);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) Ost[(32 * half + t) * 129 + j] = v[t];
+            for (int t = 0; t < 32; ++t) Ost[(32 * half + t) * OST + j] = v[t];
         }
         __syncthreads();
-        {
-            const int r = tid >> 2, part = tid & 3;  // 4 threads per token, 32 channels each
-            float ss = 0.f;
-#pragma unroll 8
-            for (int t = 0; t < 32; ++t) {
-                const float o = Ost[r * 129 + 32 * part + t];
-                ss = fmaf(o, o, ss);
-            }
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8) {  // one warp per token, 4 contiguous channels per lane
+            const int r = warp + 8 * k8;
+            const float4 o4 = *reinterpret_cast<const float4 *>(Ost + r * OST + 4 * lane);
+            float ss = o4.x * o4.x;
+            ss = fmaf(o4.y, o4.y, ss);
+            ss = fmaf(o4.z, o4.z, ss);
+            ss = fmaf(o4.w, o4.w, ss);
+            ss = warp_sum(ss);
             const float rr = rsqrtf(ss * (1.0f / D) + a.rms_eps);
             if (r < e.n) {
-                const size_t base = ((size_t)(e.t0 + r) * H + h) * D + 32 * part;
-                uint4 yo[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t zw[4] = {zr[u].x, zr[u].y, zr[u].z, zr[u].w};
-                    uint32_t yw[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int jj = 32 * part + 8 * u + 2 * q;
-                        float y0 = Ost[r * 129 + jj] * rr * nw[jj];
-                        float y1 = Ost[r * 129 + jj + 1] * rr * nw[jj + 1];
-                        if (a.z) {
-                            y0 *= sigmoidf_(bf2f((uint16_t)(zw[q] & 0xffff)));
-                            y1 *= sigmoidf_(bf2f((uint16_t)(zw[q] >> 16)));
-                        }
-                        yw[q] = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
-                    }
-                    yo[u] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+                const float4 w4 = *reinterpret_cast<const float4 *>(nw + 4 * lane);
+                float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
+                if (a.z) {
+                    y0 *= sigmoid_gate(bf2f((uint16_t)(zr[k8].x & 0xffff)));
+                    y1 *= sigmoid_gate(bf2f((uint16_t)(zr[k8].x >> 16)));
+                    y2 *= sigmoid_gate(bf2f((uint16_t)(zr[k8].y & 0xffff)));
+                    y3 *= sigmoid_gate(bf2f((uint16_t)(zr[k8].y >> 16)));
                 }
-                uint4 *yp = reinterpret_cast<uint4 *>(a.y + base);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) yp[u] = yo[u];
+                *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
+                    make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
+                               (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
             }
         }
         // new state: bf16 operand tile for the next chunk; checkpoint when this chunk ends on a boundary
