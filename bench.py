@@ -352,6 +352,9 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
     e2e_val = dec_tokens * K / (e2e_ms / 1000.0)
 
+    # ---- the same decode step on a bf16 state pool
+    decode_bf16 = run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws)
+
     # ---- chunked prefill workload
     prefill = run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
 
@@ -371,6 +374,7 @@ def run_gpu(args):
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": K,
+            "decode_bf16_state": decode_bf16,
             "prefill": prefill}
     if rank == 0:
         if ws == 1 and not args.no_cpu_baseline:
@@ -379,6 +383,49 @@ def run_gpu(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws):
+    """The decode-step workload on a bf16 state pool (states stored in bf16, computed in fp32): 32 KiB of
+    state per (request, head) instead of 64 KiB."""
+    pool = kda.StatePool.empty(DEC_SLOTS, H, DK, DV, W, device=dev, state_dtype=torch.bfloat16)
+    ki.fill_device_pool(pool.S, pool.conv, seed)
+    K, Wm = max(3, min(args.steps, 1000)), args.warmup
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed + 1)
+    slots = torch.rand(K + Wm, DEC_SLOTS, device=dev, generator=g).argsort(dim=1)[:, :DEC_N].to(torch.int32)
+    slots = slots.contiguous()
+    y = torch.empty(DEC_N, H, DV, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def dec(i, st=stream):
+        s_ = slots[i]
+        kda.kda_decode_step(pool, prm, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y, s_, s_, status, st)
+
+    for i in range(Wm):
+        dec(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(K):
+            dec(Wm + i, None)
+    graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws) / K
+    del graph
+    if int(status.item()) != 0:
+        return {"error": f"device status {int(status.item())}"}
+    per_ht = 2 * DK * DV * 2 + 2 * (W - 1) * (2 * DK + DV) * 2 + (3 * DK + DK + DV + DV) * 2 + 2
+    gbs = per_ht * DEC_N * H / (ms / 1000.0) / 1e9
+    return {"workload": "decode step as above on a bf16 state pool (4096 slots, 4 GiB)",
+            "tokens_per_s": DEC_N * ws / (ms / 1000.0), "ms_per_step": ms, "steps": K,
+            "algorithmic_bytes_per_launch": per_ht * DEC_N * H, "achieved_gbs": gbs, "hbm_frac": gbs / hbm_peak}
 
 
 def prefill_problem(seed: int, lens, chunk: int, interval: int, num_slots: int):

@@ -30,9 +30,13 @@ class KdaError(RuntimeError):
         self.rc = rc
 
 
+KDA_STATE_FP32, KDA_STATE_BF16 = 0, 1
+
+
 class _Pool(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("conv_w", ctypes.c_int32),
-                ("num_slots", ctypes.c_int64), ("S", ctypes.c_void_p), ("conv", ctypes.c_void_p)]
+                ("state_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32), ("num_slots", ctypes.c_int64),
+                ("S", ctypes.c_void_p), ("conv", ctypes.c_void_p)]
 
 
 class _Params(ctypes.Structure):
@@ -90,18 +94,25 @@ def _stream(stream):
 
 @dataclass
 class StatePool:
-    """The state-slot pool: S [num_slots, H, dk, dv] fp32 and conv [num_slots, H, W-1, 2dk+dv] bf16."""
+    """The state-slot pool: S [num_slots, H, dk, dv] fp32 or bf16, conv [num_slots, H, W-1, 2dk+dv] bf16."""
     S: torch.Tensor
     conv: torch.Tensor
 
     @staticmethod
-    def empty(num_slots: int, H: int, dk: int, dv: int, W: int = 4, device="cuda") -> "StatePool":
-        return StatePool(torch.zeros(num_slots, H, dk, dv, dtype=torch.float32, device=device),
+    def empty(num_slots: int, H: int, dk: int, dv: int, W: int = 4, device="cuda",
+              state_dtype=torch.float32) -> "StatePool":
+        return StatePool(torch.zeros(num_slots, H, dk, dv, dtype=state_dtype, device=device),
                          torch.zeros(num_slots, H, W - 1, 2 * dk + dv, dtype=torch.bfloat16, device=device))
 
     def c(self) -> _Pool:
         ns, H, dk, dv = self.S.shape
-        return _Pool(H, dk, dv, self.conv.shape[2] + 1, ns, _ptr(self.S), _ptr(self.conv))
+        if self.S.dtype == torch.float32:
+            sd = KDA_STATE_FP32
+        elif self.S.dtype == torch.bfloat16:
+            sd = KDA_STATE_BF16
+        else:
+            raise TypeError("state pool dtype must be float32 or bfloat16")
+        return _Pool(H, dk, dv, self.conv.shape[2] + 1, sd, 0, ns, _ptr(self.S), _ptr(self.conv))
 
 
 @dataclass

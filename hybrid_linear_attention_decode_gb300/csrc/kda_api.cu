@@ -27,6 +27,7 @@ static bool aligned2(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 1
 static int check_pool(const kda_pool *pool, const kda_params *prm) {
     if (!pool || !pool->S || !pool->conv || pool->H <= 0 || pool->num_slots <= 0 || pool->dk <= 0 || pool->dv <= 0)
         return KDA_ERR_INVALID_ARG;
+    if (pool->state_dtype != KDA_STATE_FP32 && pool->state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
     if (!aligned16(pool->S) || !aligned16(pool->conv)) return KDA_ERR_INVALID_ARG;
     if (prm) {
         if (!prm->conv_weight || !prm->norm_weight) return KDA_ERR_INVALID_ARG;
@@ -76,6 +77,7 @@ int kda_decode_step(const kda_pool *pool, const kda_params *prm, int32_t n, cons
         return KDA_ERR_INVALID_ARG;
     DecodeArgs d;
     d.S = pool->S;
+    d.state_bf16 = pool->state_dtype == KDA_STATE_BF16;
     d.conv = pool->conv;
     d.num_slots = pool->num_slots;
     d.H = pool->H;
@@ -124,6 +126,7 @@ int kda_prefill_chunked(const kda_pool *pool, const kda_params *prm, int32_t nse
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
     PrefillArgs p;
     p.S = pool->S;
+    p.state_bf16 = pool->state_dtype == KDA_STATE_BF16;
     p.conv = pool->conv;
     p.num_slots = pool->num_slots;
     p.H = pool->H;
@@ -158,7 +161,7 @@ int kda_resume_from_slot(const kda_pool *pool, int32_t n, const int32_t *src_slo
     if (n == 0) return KDA_OK;
     if (!src_slot || !dst_slot || !aligned4(src_slot) || !aligned4(dst_slot)) return KDA_ERR_INVALID_ARG;
     if (pool->conv_w < 1) return KDA_ERR_INVALID_ARG;
-    const int64_t s_bytes = (int64_t)pool->dk * pool->dv * 4;
+    const int64_t s_bytes = (int64_t)pool->dk * pool->dv * (pool->state_dtype == KDA_STATE_BF16 ? 2 : 4);
     const int64_t c_bytes = (int64_t)(pool->conv_w - 1) * (2 * pool->dk + pool->dv) * 2;
     if (s_bytes % 16 || c_bytes % 16) return KDA_ERR_UNSUPPORTED_SHAPE;
     ResumeArgs r;

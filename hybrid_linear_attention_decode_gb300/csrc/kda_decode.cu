@@ -22,8 +22,17 @@
 
 namespace kda {
 
-template <int DK, int DV, int NBUF>
+// Resident CTAs per SM targeted for a bf16 pool at dk = dv = 128 (the register budget follows from it).
+#ifndef KDA_DECODE_BF16_CTAS
+#define KDA_DECODE_BF16_CTAS 3
+#endif
+#ifndef KDA_DECODE_NBUF_BF16
+#define KDA_DECODE_NBUF_BF16 1
+#endif
+
+template <int DK, int DV, int NBUF, bool SBF>
 struct DecodeShape {
+    static constexpr int ES = SBF ? 2 : 4;    // bytes per stored state element (bf16 or fp32 pool)
     static constexpr int W = 4;
     static constexpr int CC = 2 * DK + DV;
     static constexpr int NT = (DK * DV >= 4096) ? 256 : 64;
@@ -33,7 +42,7 @@ struct DecodeShape {
     static constexpr int NST = (DK >= 128) ? 4 : 1;
     static constexpr int M_ST = RPT / NST;    // rows per thread per stage
     static constexpr int CPT = (CC + NT - 1) / NT;  // conv channels per thread
-    static constexpr uint32_t S_BYTES = DK * DV * 4;
+    static constexpr uint32_t S_BYTES = DK * DV * ES;
     static constexpr uint32_t ST_BYTES = S_BYTES / NST;
     static constexpr uint32_t CONV_BYTES = (W - 1) * CC * 2;
     static constexpr uint32_t OFF_CONV = S_BYTES;
@@ -47,7 +56,7 @@ struct DecodeShape {
     static constexpr uint32_t OFF_F = NBUF * BUF_BYTES;
     static constexpr uint32_t OFF_BAR = (OFF_F + NF * 4 + 15) / 16 * 16;
     static constexpr uint32_t SMEM = OFF_BAR + NBUF * (1 + NST) * 8;
-    static constexpr int MIN_BLOCKS = (NBUF == 1 && DK * DV >= 4096) ? 2 : 1;
+    static constexpr int MIN_BLOCKS = (DK * DV >= 4096) ? (SBF ? KDA_DECODE_BF16_CTAS : (NBUF == 1 ? 2 : 1)) : 1;
 
     static_assert(LPR <= 32 && 32 % LPR == 0, "row mapping");
     static_assert(DV <= NT, "one output channel per thread in the epilogue");
@@ -56,10 +65,10 @@ struct DecodeShape {
     static_assert(OFF_CONV % 16 == 0 && OFF_Q % 16 == 0 && OFF_V % 16 == 0 && OFF_A % 16 == 0, "align");
 };
 
-template <int DK, int DV, int NBUF>
-__global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT, DecodeShape<DK, DV, NBUF>::MIN_BLOCKS)
+template <int DK, int DV, int NBUF, bool SBF>
+__global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF, SBF>::NT, DecodeShape<DK, DV, NBUF, SBF>::MIN_BLOCKS)
     kda_decode_kernel(const DecodeArgs args) {
-    using C = DecodeShape<DK, DV, NBUF>;
+    using C = DecodeShape<DK, DV, NBUF, SBF>;
     constexpr int NT = C::NT, CC = C::CC, NST = C::NST, RPP = C::RPP, LPR = C::LPR, RPT = C::RPT;
     extern __shared__ __align__(128) uint8_t smem[];
     float *red_k = reinterpret_cast<float *>(smem + C::OFF_F);  // [RPP][DV]
@@ -114,7 +123,7 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT, DecodeShape<DK,
         if (src >= 0) {
             const size_t sh = (size_t)src * H + h;
             bulk_g2s(bp + C::OFF_CONV, args.conv + sh * (C::W - 1) * CC, C::CONV_BYTES, bi);
-            const uint8_t *gS = reinterpret_cast<const uint8_t *>(args.S + sh * DK * DV);
+            const uint8_t *gS = reinterpret_cast<const uint8_t *>(args.S) + sh * C::S_BYTES;
             for (int s = 0; s < NST; ++s) {
                 mbar_arrive_expect_tx(&bs[s], C::ST_BYTES);
                 bulk_g2s(bp + s * C::ST_BYTES, gS + (size_t)s * C::ST_BYTES, C::ST_BYTES, &bs[s]);
@@ -212,7 +221,8 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT, DecodeShape<DK,
         __syncthreads();
 
         // ---- pass 1: the state into registers; column sums of k^T S' and q^T S' ----
-        float4 sr[RPT];
+        float4 sr[SBF ? 1 : RPT];   // fp32 pool: the state slice in registers
+        uint2 sh[SBF ? RPT : 1];    // bf16 pool: the same slice as packed bf16 pairs
         float4 accK = make_float4(0.f, 0.f, 0.f, 0.f), accQ = accK;
         bool sfail = false;
         if (src >= 0) {
@@ -223,8 +233,16 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT, DecodeShape<DK,
                 for (int m = 0; m < C::M_ST; ++m) {
                     const int mm = s * C::M_ST + m;
                     const int row = g + mm * RPP;
-                    const float4 x = *reinterpret_cast<const float4 *>(Ss + row * DV + cg * 4);
-                    sr[mm] = x;
+                    float4 x;
+                    if (SBF) {
+                        const uint2 hb = *reinterpret_cast<const uint2 *>(bp + (row * DV + cg * 4) * 2);
+                        sh[mm] = hb;
+                        x = make_float4(bf2f((uint16_t)(hb.x & 0xffff)), bf2f((uint16_t)(hb.x >> 16)),
+                                        bf2f((uint16_t)(hb.y & 0xffff)), bf2f((uint16_t)(hb.y >> 16)));
+                    } else {
+                        x = *reinterpret_cast<const float4 *>(Ss + row * DV + cg * 4);
+                        sr[mm] = x;
+                    }
                     const float kk = ka[row], qq = qa[row];
                     accK.x = fmaf(kk, x.x, accK.x); accK.y = fmaf(kk, x.y, accK.y);
                     accK.z = fmaf(kk, x.z, accK.z); accK.w = fmaf(kk, x.w, accK.w);
@@ -234,7 +252,10 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT, DecodeShape<DK,
             }
         } else {
 #pragma unroll
-            for (int mm = 0; mm < RPT; ++mm) sr[mm] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int mm = 0; mm < RPT; ++mm) {
+                if (SBF) sh[mm] = make_uint2(0u, 0u);
+                else sr[mm] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         *reinterpret_cast<float4 *>(red_k + g * DV + cg * 4) = accK;
         *reinterpret_cast<float4 *>(red_q + g * DV + cg * 4) = accQ;
@@ -263,27 +284,40 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF>::NT, DecodeShape<DK,
         const float rr = rsqrtf(ss * (1.0f / DV) + args.rms_eps);
         for (int j = tid; j < DV; j += NT) args.y[th * DV + j] = f2bf(os[j] * rr * nw[j] * zg);
         // ---- pass 2: S_new = Diag(alpha) S + k^ (beta u)^T from registers, 128-bit stores ----
-        float *Sd = args.S + ((size_t)dst * H + h) * DK * DV;
+        uint8_t *Sd = reinterpret_cast<uint8_t *>(args.S) + ((size_t)dst * H + h) * C::S_BYTES;
         const float4 b4 = *reinterpret_cast<const float4 *>(bu + cg * 4);
 #pragma unroll
         for (int mm = 0; mm < RPT; ++mm) {
             const int row = g + mm * RPP;
             const float aa = al[row], kk = kh[row];
-            const float4 x = sr[mm];
+            float4 x;
+            if (SBF) {
+                const uint2 hb = sh[mm];
+                x = make_float4(bf2f((uint16_t)(hb.x & 0xffff)), bf2f((uint16_t)(hb.x >> 16)),
+                                bf2f((uint16_t)(hb.y & 0xffff)), bf2f((uint16_t)(hb.y >> 16)));
+            } else {
+                x = sr[mm];
+            }
             float4 o4;
             o4.x = fmaf(kk, b4.x, aa * x.x);
             o4.y = fmaf(kk, b4.y, aa * x.y);
             o4.z = fmaf(kk, b4.z, aa * x.z);
             o4.w = fmaf(kk, b4.w, aa * x.w);
-            *reinterpret_cast<float4 *>(Sd + row * DV + cg * 4) = o4;
+            if (SBF) {
+                *reinterpret_cast<uint2 *>(Sd + (row * DV + cg * 4) * 2) =
+                    make_uint2((uint32_t)f2bf(o4.x) | ((uint32_t)f2bf(o4.y) << 16),
+                               (uint32_t)f2bf(o4.z) | ((uint32_t)f2bf(o4.w) << 16));
+            } else {
+                *reinterpret_cast<float4 *>(Sd + (row * DV + cg * 4) * 4) = o4;
+            }
         }
     }
 }
 
-template <int DK, int DV, int NBUF>
+template <int DK, int DV, int NBUF, bool SBF>
 static int launch_decode_t(const DecodeArgs &a, cudaStream_t st) {
-    using C = DecodeShape<DK, DV, NBUF>;
-    auto kern = kda_decode_kernel<DK, DV, NBUF>;
+    using C = DecodeShape<DK, DV, NBUF, SBF>;
+    auto kern = kda_decode_kernel<DK, DV, NBUF, SBF>;
     static int occ_cache[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_CUDA;
@@ -313,12 +347,17 @@ bool decode_supported(int dk, int dv, int W) {
 #define KDA_DECODE_NBUF_128 1
 #endif
 
+template <int DK, int DV, int NBUF_F32, int NBUF_BF16>
+static int launch_decode_dt(const DecodeArgs &a, cudaStream_t st) {
+    return a.state_bf16 ? launch_decode_t<DK, DV, NBUF_BF16, true>(a, st) : launch_decode_t<DK, DV, NBUF_F32, false>(a, st);
+}
+
 int launch_decode(const DecodeArgs &a, int dk, int dv, cudaStream_t st) {
-    if (dk == 128 && dv == 128) return launch_decode_t<128, 128, KDA_DECODE_NBUF_128>(a, st);
-    if (dk == 64 && dv == 64) return launch_decode_t<64, 64, 2>(a, st);
-    if (dk == 16 && dv == 16) return launch_decode_t<16, 16, 2>(a, st);
-    if (dk == 32 && dv == 16) return launch_decode_t<32, 16, 2>(a, st);
-    if (dk == 16 && dv == 32) return launch_decode_t<16, 32, 2>(a, st);
+    if (dk == 128 && dv == 128) return launch_decode_dt<128, 128, KDA_DECODE_NBUF_128, KDA_DECODE_NBUF_BF16>(a, st);
+    if (dk == 64 && dv == 64) return launch_decode_dt<64, 64, 2, 2>(a, st);
+    if (dk == 16 && dv == 16) return launch_decode_dt<16, 16, 2, 2>(a, st);
+    if (dk == 32 && dv == 16) return launch_decode_dt<32, 16, 2, 2>(a, st);
+    if (dk == 16 && dv == 32) return launch_decode_dt<16, 32, 2, 2>(a, st);
     return KDA_ERR_UNSUPPORTED_SHAPE;
 }
 

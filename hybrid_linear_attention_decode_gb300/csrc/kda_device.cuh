@@ -109,6 +109,17 @@ __device__ __forceinline__ float warp_dot_array(const float *x, const float *y, 
     return warp_sum(s);
 }
 
+// Pool state element access for an fp32 or a bf16 pool (bf16: round to nearest even on store).
+__device__ __forceinline__ float load_state(const void *S, bool bf, size_t idx) {
+    return bf ? bf2f(reinterpret_cast<const uint16_t *>(S)[idx]) : reinterpret_cast<const float *>(S)[idx];
+}
+__device__ __forceinline__ void store_state(void *S, bool bf, size_t idx, float v) {
+    if (bf)
+        reinterpret_cast<uint16_t *>(S)[idx] = f2bf(v);
+    else
+        reinterpret_cast<float *>(S)[idx] = v;
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }

@@ -10,7 +10,8 @@
 namespace kda {
 
 struct DecodeArgs {
-    float *S;            // pool states [num_slots][H][dk][dv]
+    void *S;             // pool states [num_slots][H][dk][dv], fp32 or bf16 (state_bf16)
+    int32_t state_bf16;
     uint16_t *conv;      // pool windows [num_slots][H][W-1][2dk+dv]
     int64_t num_slots;
     int32_t H, n;
@@ -24,7 +25,7 @@ struct DecodeArgs {
 };
 
 struct ResumeArgs {
-    float *S;
+    void *S;
     uint16_t *conv;
     int64_t num_slots;
     int32_t H, n;
@@ -35,7 +36,8 @@ struct ResumeArgs {
 };
 
 struct PrefillArgs {
-    float *S;
+    void *S;             // fp32 or bf16 (state_bf16)
+    int32_t state_bf16;
     uint16_t *conv;
     int64_t num_slots;
     int32_t H, nseq;

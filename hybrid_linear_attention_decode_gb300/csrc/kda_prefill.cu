@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(const PrefillAr
     float *gl = U + C * DVT;       // [dk]
     for (int idx = tid; idx < dk * DVT; idx += kThreads) {
         const int i = idx / DVT, j = idx - (idx / DVT) * DVT;
-        S[idx] = src >= 0 ? a.S[(((size_t)src * H + h) * dk + i) * dv + j0 + j] : 0.f;
+        S[idx] = src >= 0 ? load_state(a.S, a.state_bf16, (((size_t)src * H + h) * dk + i) * dv + j0 + j) : 0.f;
     }
     const int64_t start = a.start_pos[n];
     const int32_t c0 = wsp<int32_t>(a, L.off_seqc)[n], c1 = wsp<int32_t>(a, L.off_seqc)[n + 1];
@@ -413,14 +413,14 @@ __global__ void __launch_bounds__(kThreads) prefill_state_kernel(const PrefillAr
             if (s >= 0 && s < a.num_slots) {
                 for (int idx = tid; idx < dk * DVT; idx += kThreads) {
                     const int i = idx / DVT, jj = idx - (idx / DVT) * DVT;
-                    a.S[(((size_t)s * H + h) * dk + i) * dv + j0 + jj] = S[idx];
+                    store_state(a.S, a.state_bf16, (((size_t)s * H + h) * dk + i) * dv + j0 + jj, S[idx]);
                 }
             }
         }
     }
     for (int idx = tid; idx < dk * DVT; idx += kThreads) {
         const int i = idx / DVT, j = idx - (idx / DVT) * DVT;
-        a.S[(((size_t)dst * H + h) * dk + i) * dv + j0 + j] = S[idx];
+        store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * dk + i) * dv + j0 + j, S[idx]);
     }
     if (c0 == c1 && blockIdx.z == 0) {  // empty sequence: the window passes through unchanged
         const int CC = 2 * dk + dv;
@@ -1033,7 +1033,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
             const int i0 = 64 * half + 32 * part;
 #pragma unroll
             for (int t = 0; t < 32; ++t)
-                v[t] = src >= 0 ? a.S[(((size_t)src * H + h) * D + i0 + t) * D + j] : 0.f;
+                v[t] = src >= 0 ? load_state(a.S, a.state_bf16, (((size_t)src * H + h) * D + i0 + t) * D + j) : 0.f;
             umma::st32(tmem + lane_off + T_S + i0, v);
 #pragma unroll
             for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
@@ -1168,7 +1168,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
                 for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
                 if (ck >= 0) {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) a.S[(((size_t)ck * H + h) * D + i0 + t) * D + j] = v[t];
+                    for (int t = 0; t < 32; ++t)
+                        store_state(a.S, a.state_bf16, (((size_t)ck * H + h) * D + i0 + t) * D + j, v[t]);
                 }
             }
         }
@@ -1182,7 +1183,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
             const int i0 = 64 * half + 32 * part;
             umma::ld32(tmem + lane_off + T_S + i0, v);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) a.S[(((size_t)dst * H + h) * D + i0 + t) * D + j] = v[t];
+            for (int t = 0; t < 32; ++t)
+                store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
         }
         if (c0 == c1) {  // empty sequence: the window passes through unchanged
             uint16_t *cw = a.conv + ((size_t)dst * H + h) * (kConvW - 1) * CC;

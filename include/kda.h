@@ -62,14 +62,21 @@ enum kda_status {
 /*
  * The state-slot pool ("The Hardest Part: Prefix Caching for KDA": the physical state block is
  * decoupled from the prefix-match unit; a slot here is one state snapshot).  Layout, slot-major:
- *   S    [num_slots][H][dk][dv]         fp32, row i = key channel, column j = value channel
+ *   S    [num_slots][H][dk][dv]         state_dtype (fp32, or bf16 bit patterns); row i = key channel,
+ *                                       column j = value channel
  *   conv [num_slots][H][W-1][2dk+dv]    bf16, the last W-1 RAW (pre-conv) q|k|v inputs, oldest first
- * Both device, owned by the caller.
+ * Both device, owned by the caller.  With a bf16 pool ("moonshotai/Kimi-K3" recipe:
+ * --mamba-ssm-cache-dtype bfloat16) every kernel computes in fp32 and rounds the state to bf16 (nearest
+ * even) where it is stored; this halves the state bytes of a decode step.
  */
+enum kda_state_dtype { KDA_STATE_FP32 = 0, KDA_STATE_BF16 = 1 };
+
 typedef struct kda_pool {
     int32_t H, dk, dv, conv_w;  /* heads, key dim, value dim, conv width W */
+    int32_t state_dtype;        /* enum kda_state_dtype */
+    int32_t reserved;           /* 0 */
     int64_t num_slots;
-    float *S;
+    void *S;
     uint16_t *conv;
 } kda_pool;
 

@@ -167,6 +167,18 @@ def forward(cfg: Cfg, cu_seqlens, start_pos, q, k, v, a, b, z, conv_w, norm_w, S
                 ckpt_seq=np.array(seqs, dtype=np.int64), ckpt_pos=np.array(poss, dtype=np.int64))
 
 
+def round_to_bf16(x) -> np.ndarray:
+    """Value of x stored in a bf16 state pool: fp64 -> fp32 (nearest even) -> bf16 (nearest even)."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + ((u >> 16) & 1) + 0x7FFF) >> 16).astype(np.uint32) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64).reshape(np.shape(x))
+
+
+def _store(x, state_bf16: bool):
+    return round_to_bf16(x) if state_bf16 else x
+
+
 def _gather(pool_S, pool_conv, src):
     """Initial states of the requests: slot src[n], or zeros when src[n] == -1."""
     N = len(src)
@@ -179,11 +191,13 @@ def _gather(pool_S, pool_conv, src):
     return S0, C0
 
 
-def decode_pool(cfg: Cfg, pool_S, pool_conv, src_slot, dst_slot, q, k, v, a, b, z, conv_w, norm_w) -> dict:
+def decode_pool(cfg: Cfg, pool_S, pool_conv, src_slot, dst_slot, q, k, v, a, b, z, conv_w, norm_w,
+                state_bf16: bool = False) -> dict:
     """One decode token per request on a slot pool.
 
     pool_S [slots,H,dk,dv] and pool_conv [slots,H,W-1,Cc] are taken as values (any float dtype); returns
-    the fp64 pools after the step (only dst slots change), plus o and y [N,H,dv].
+    the fp64 pools after the step (only dst slots change), plus o and y [N,H,dv].  With state_bf16 the
+    pool stores states in bf16: a written state is rounded to bf16 (nearest even).
     """
     N = len(src_slot)
     S0, C0 = _gather(pool_S, pool_conv, src_slot)
@@ -191,13 +205,13 @@ def decode_pool(cfg: Cfg, pool_S, pool_conv, src_slot, dst_slot, q, k, v, a, b, 
     out_S = np.array(pool_S, dtype=np.float64, copy=True)
     out_C = np.array(pool_conv, dtype=np.float64, copy=True)
     for n, d in enumerate(dst_slot):
-        out_S[d] = r["S"][n]
+        out_S[d] = _store(r["S"][n], state_bf16)
         out_C[d] = r["conv"][n]
     return dict(pool_S=out_S, pool_conv=out_C, o=r["o"], y=r["y"])
 
 
 def prefill_pool(cfg: Cfg, pool_S, pool_conv, cu_seqlens, start_pos, src_slot, dst_slot, interval,
-                 ckpt_slots, q, k, v, a, b, z, conv_w, norm_w, chunk: int = 0) -> dict:
+                 ckpt_slots, q, k, v, a, b, z, conv_w, norm_w, chunk: int = 0, state_bf16: bool = False) -> dict:
     """Varlen prefill on a slot pool with checkpoint emission.
 
     ckpt_slots lists one slot (or -1 = skip) per boundary, sequences in order, boundaries ascending.
@@ -212,10 +226,10 @@ def prefill_pool(cfg: Cfg, pool_S, pool_conv, cu_seqlens, start_pos, src_slot, d
     out_C = np.array(pool_conv, dtype=np.float64, copy=True)
     for j, s in enumerate(ckpt_slots):
         if s >= 0:
-            out_S[s] = r["ckpt_S"][j]
+            out_S[s] = _store(r["ckpt_S"][j], state_bf16)
             out_C[s] = r["ckpt_conv"][j]
     for n, d in enumerate(dst_slot):
-        out_S[d] = r["S"][n]
+        out_S[d] = _store(r["S"][n], state_bf16)
         out_C[d] = r["conv"][n]
     return dict(pool_S=out_S, pool_conv=out_C, o=r["o"], y=r["y"], ckpt_seq=r["ckpt_seq"],
                 ckpt_pos=r["ckpt_pos"], ckpt_S=r["ckpt_S"], ckpt_conv=r["ckpt_conv"])

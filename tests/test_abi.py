@@ -57,14 +57,17 @@ def test_host_validation_without_gpu(lib):
     # NULL pool / params: rejected before any CUDA call
     assert lib.kda_decode_step(None, None, 1, *([None] * 11)) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_resume_from_slot(None, 1, None, None, None, None) == kda.KDA_ERR_INVALID_ARG
-    pool = kda._Pool(2, 128, 128, 4, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
+    pool = kda._Pool(2, 128, 128, 4, 0, 0, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
     # unsupported shape / misaligned pointers are host errors
-    bad = kda._Pool(2, 96, 128, 4, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
+    bad = kda._Pool(2, 96, 128, 4, 0, 0, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
     prm = kda._Params(ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000), 1e-6, 1e-6, 1.0, 1)
     assert lib.kda_decode_step(ctypes.byref(bad), ctypes.byref(prm), 1, *([None] * 11)) == \
         kda.KDA_ERR_UNSUPPORTED_SHAPE
-    mis = kda._Pool(2, 128, 128, 4, 8, ctypes.c_void_p(0x1004), ctypes.c_void_p(0x2000))
+    mis = kda._Pool(2, 128, 128, 4, 0, 0, 8, ctypes.c_void_p(0x1004), ctypes.c_void_p(0x2000))
     assert lib.kda_decode_step(ctypes.byref(mis), ctypes.byref(prm), 1, *([None] * 11)) == kda.KDA_ERR_INVALID_ARG
+    # an unknown state dtype is an invalid argument
+    odd = kda._Pool(2, 128, 128, 4, 7, 0, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
+    assert lib.kda_decode_step(ctypes.byref(odd), ctypes.byref(prm), 1, *([None] * 11)) == kda.KDA_ERR_INVALID_ARG
     # n = 0 is a no-op that returns OK without touching the device
     assert lib.kda_decode_step(ctypes.byref(pool), ctypes.byref(prm), 0, *([None] * 11)) == kda.KDA_OK
     assert lib.kda_resume_from_slot(ctypes.byref(pool), 0, None, None, None, None) == kda.KDA_OK

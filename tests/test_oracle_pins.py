@@ -369,3 +369,13 @@ def test_golden_tiny_regression_anchor():
     for key, val in now.items():
         np.testing.assert_allclose(np.asarray(val, dtype=np.float64), np.asarray(ref[key], dtype=np.float64),
                                    rtol=1e-12, atol=1e-14, err_msg=key)
+
+
+def test_bf16_pool_rounding_is_nearest_even():
+    """The oracle's bf16-pool storage rounds to nearest even: a tie goes to the even neighbour, a value
+    just above a tie rounds up, and values already representable in bf16 are unchanged."""
+    x = np.array([1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -8 + 2.0 ** -20, -2.5, 0.0])
+    want = np.array([1.0, 1.0, 1.0 + 2.0 ** -6, 1.0 + 2.0 ** -7, -2.5, 0.0])
+    np.testing.assert_array_equal(oracle.round_to_bf16(x), want)
+    vals = ki.bf16_bits_to_f64(ki.f32_to_bf16_bits(RNG.standard_normal(1000).astype(np.float32)))
+    np.testing.assert_array_equal(oracle.round_to_bf16(vals), vals)

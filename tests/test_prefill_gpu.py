@@ -10,8 +10,8 @@ import torch
 
 import kda_inputs as ki
 import oracle
-from tests.kda_testutil import (S_TOL, Y_TOL, bf16_dev_bits, bf16_dev_to_f64, fill_pool, pool_unit_host, s_err,
-                                to_dev_bf16, y_err)
+from tests.kda_testutil import (S_TOL, S_TOL_BF16, Y_TOL, bf16_dev_bits, bf16_dev_to_f64, fill_pool, pool_unit_host,
+                                s_err, to_dev_bf16, y_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -26,13 +26,14 @@ class Problem:
     """A varlen prefill call: sequences, start positions, slots, checkpoint table, inputs."""
 
     def __init__(self, kda, H, dk, dv, lens, starts, src, dst, chunk, interval, num_slots, seed, with_z=True,
-                 fill=True, ckpt_skip=()):
-        self.kda, self.H, self.dk, self.dv = kda, H, dk, dv
+                 fill=True, ckpt_skip=(), sbf16=False):
+        self.kda, self.H, self.dk, self.dv, self.sbf16 = kda, H, dk, dv, sbf16
         self.lens, self.starts, self.src, self.dst = list(lens), list(starts), list(src), list(dst)
         self.chunk, self.interval, self.num_slots = chunk, interval, num_slots
         self.T = int(sum(lens))
         self.cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
-        self.pool = kda.StatePool.empty(num_slots, H, dk, dv)
+        self.pool = kda.StatePool.empty(num_slots, H, dk, dv,
+                                        state_dtype=torch.bfloat16 if sbf16 else torch.float32)
         self.S_h, self.C_h = fill_pool(self.pool, seed) if fill else (None, None)
         self.wts = ki.layer_weights(seed, H, dk, dv)
         self.prm = kda.LayerParams(torch.from_numpy(self.wts["conv_w"]).cuda(),
@@ -76,6 +77,8 @@ class Problem:
             if s >= 0:
                 Sa, Ca = pool_unit_host(self.S_h, self.C_h, s, self.H)
                 S0[n], C0[n] = Sa[heads], Ca[heads]
+                if self.sbf16:  # the pool holds the bf16 rounding of the generated states
+                    S0[n] = oracle.round_to_bf16(S0[n])
         f = {k: (ki.bf16_bits_to_f64(v)[:, heads] if v is not None else None) for k, v in self.tok.items()}
         return oracle.forward(cfg, self.cu, np.array(self.starts, dtype=np.int64), f["q"], f["k"], f["v"], f["a"],
                               f["b"], f["z"], self.wts["conv_w"][heads], self.wts["norm_w"], S0, C0,
@@ -83,18 +86,19 @@ class Problem:
 
     def check(self, ref, heads=None):
         heads = list(range(self.H)) if heads is None else list(heads)
+        stol = S_TOL_BF16 if self.sbf16 else S_TOL
         yg = bf16_dev_to_f64(self.y)[:, heads]
         assert y_err(yg, ref["y"]) <= Y_TOL
         for n, d in enumerate(self.dst):
-            Sg = self.pool.S[d].cpu().numpy()[heads]
-            assert s_err(Sg, ref["S"][n]) <= S_TOL, ("final", n)
+            Sg = self.pool.S[d].float().cpu().numpy()[heads]
+            assert s_err(Sg, ref["S"][n]) <= stol, ("final", n)
             np.testing.assert_array_equal(ki.bf16_bits_to_f64(bf16_dev_bits(self.pool.conv[d]))[heads],
                                           ref["conv"][n])
         for j, slot in enumerate(self.ck):
             if slot < 0:
                 continue
-            Sg = self.pool.S[int(slot)].cpu().numpy()[heads]
-            assert s_err(Sg, ref["ckpt_S"][j]) <= S_TOL, ("ckpt", j, int(ref["ckpt_pos"][j]))
+            Sg = self.pool.S[int(slot)].float().cpu().numpy()[heads]
+            assert s_err(Sg, ref["ckpt_S"][j]) <= stol, ("ckpt", j, int(ref["ckpt_pos"][j]))
             np.testing.assert_array_equal(ki.bf16_bits_to_f64(bf16_dev_bits(self.pool.conv[int(slot)]))[heads],
                                           ref["ckpt_conv"][j])
 
