@@ -6,7 +6,7 @@ is missing the import of an entry point raises.
 
 Entry points (same names as the C ABI): ``kda_decode_step``, ``kda_prefill_chunked``,
 ``kda_resume_from_slot``, ``kda_prefill_workspace_bytes``, ``kda_checkpoint_count``,
-``kda_status_string``.
+``kda_status_string``; the host prefix index ``kda_prefix_*`` through :class:`PrefixIndex`.
 """
 from __future__ import annotations
 
@@ -44,6 +44,14 @@ class _Params(ctypes.Structure):
                 ("rms_eps", ctypes.c_float), ("scale", ctypes.c_float), ("conv_silu", ctypes.c_int32)]
 
 
+class _PrefixPlan(ctypes.Structure):
+    _fields_ = [("plan_id", ctypes.c_uint64), ("src_slot", ctypes.c_int32), ("private_slot", ctypes.c_int32),
+                ("start_pos", ctypes.c_int64), ("num_ckpts", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+KDA_RETAIN_INTERVAL, KDA_RETAIN_SECOND_HIT = 0, 1
+
+
 def load_library(path: str | None = None):
     """Load libkda.so (built in-tree by ``hybrid_linear_attention_decode_gb300/build.py``)."""
     global _lib
@@ -71,6 +79,20 @@ def load_library(path: str | None = None):
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_version.restype = ctypes.c_int
+    lib.kda_prefix_index_create.argtypes = [i32, i32, i32, i64]
+    lib.kda_prefix_index_create.restype = vp
+    lib.kda_prefix_index_destroy.argtypes = [vp]
+    lib.kda_prefix_index_destroy.restype = None
+    lib.kda_prefix_index_free_slots.argtypes = [vp]
+    lib.kda_prefix_index_free_slots.restype = i32
+    lib.kda_prefix_plan.argtypes = [vp, vp, i64, ctypes.POINTER(_PrefixPlan), vp, i32]
+    lib.kda_prefix_plan.restype = ctypes.c_int
+    lib.kda_prefix_commit.argtypes = [vp, ctypes.c_uint64]
+    lib.kda_prefix_commit.restype = ctypes.c_int
+    lib.kda_prefix_abort.argtypes = [vp, ctypes.c_uint64]
+    lib.kda_prefix_abort.restype = ctypes.c_int
+    lib.kda_prefix_release_slot.argtypes = [vp, i32]
+    lib.kda_prefix_release_slot.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -203,3 +225,63 @@ def kda_resume_from_slot(pool: StatePool, src_slot, dst_slot, dev_status, stream
     rc = load_library().kda_resume_from_slot(ctypes.byref(pc), int(src_slot.shape[0]), _ptr(src_slot),
                                              _ptr(dst_slot), _ptr(dev_status), _stream(stream))
     _check(rc, "kda_resume_from_slot")
+
+
+@dataclass
+class PrefixPlan:
+    """What one prompt needs: resume from ``src_slot`` (or start fresh when it is -1) into ``private_slot``,
+    prefill tokens [start_pos, len) with checkpoint interval = the match unit and the ``ckpt_slots`` table
+    (one entry per match-unit boundary in (start_pos, len]: a pool slot, or -1 to skip)."""
+    plan_id: int
+    src_slot: int
+    private_slot: int
+    start_pos: int
+    ckpt_slots: list
+
+
+class PrefixIndex:
+    """Host prefix index over a state pool (``kda_prefix_index_*`` in the C ABI): chained match-unit hashes
+    to checkpoint slots, copy-on-write private slots, LRU eviction, interval or second-hit retention."""
+
+    def __init__(self, num_slots: int, match_unit: int = 128, policy: int = KDA_RETAIN_INTERVAL,
+                 interval: int = 0):
+        self._lib = load_library()
+        self._h = self._lib.kda_prefix_index_create(int(num_slots), int(match_unit), int(policy), int(interval))
+        if not self._h:
+            raise KdaError(KDA_ERR_INVALID_ARG, "kda_prefix_index_create")
+        self.match_unit = int(match_unit)
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.kda_prefix_index_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def free_slots(self) -> int:
+        return int(self._lib.kda_prefix_index_free_slots(self._h))
+
+    def plan(self, tokens) -> PrefixPlan:
+        import numpy as np
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        cap = max(1, len(t) // self.match_unit)
+        ck = np.empty(cap, dtype=np.int32)
+        out = _PrefixPlan()
+        rc = self._lib.kda_prefix_plan(self._h, t.ctypes.data_as(ctypes.c_void_p), len(t), ctypes.byref(out),
+                                       ck.ctypes.data_as(ctypes.c_void_p), cap)
+        _check(rc, "kda_prefix_plan")
+        return PrefixPlan(int(out.plan_id), int(out.src_slot), int(out.private_slot), int(out.start_pos),
+                          [int(x) for x in ck[:out.num_ckpts]])
+
+    def commit(self, plan: PrefixPlan) -> None:
+        _check(self._lib.kda_prefix_commit(self._h, plan.plan_id), "kda_prefix_commit")
+
+    def abort(self, plan: PrefixPlan) -> None:
+        _check(self._lib.kda_prefix_abort(self._h, plan.plan_id), "kda_prefix_abort")
+
+    def release_slot(self, slot: int) -> None:
+        _check(self._lib.kda_prefix_release_slot(self._h, int(slot)), "kda_prefix_release_slot")

@@ -49,7 +49,7 @@ def _compile(src: str) -> str:
 def build(verbose: bool = False) -> str:
     """Compile every kernel file for sm_103a and link libkda.so; returns its path."""
     os.makedirs(OUT, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(_compile, srcs))
     if not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):

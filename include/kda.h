@@ -182,6 +182,60 @@ KDA_API int kda_prefill_chunked_noalloc(const kda_pool *pool, const kda_params *
 KDA_API int kda_resume_from_slot(const kda_pool *pool, int32_t n, const int32_t *src_slot, const int32_t *dst_slot,
                          int32_t *dev_status, kda_stream_t stream);
 
+/*
+ * Host-side prefix index and retention policies ("A Preview of Production-Scale Kimi K3 Support on vLLM",
+ * section "The Hardest Part: Prefix Caching for KDA": chained fine-grained hashes, copy-on-write of a
+ * cached partial state into a private destination, deferred same-step reuse; "vLLM Kimi K3 Support",
+ * section "Agentic Cache Retention Policies": interval retention and Marconi-style second-hit retention;
+ * "moonshotai/Kimi-K3" recipe: prefix-match unit 128).  Pure host code: it hands out indices of the
+ * caller's state pool and fills the ckpt_slots table of kda_prefill_chunked; it allocates no device
+ * memory and makes no CUDA call.  Thread-safe (one internal mutex).
+ *
+ * A plan for a prompt of `len` tokens:
+ *   - finds the longest committed cached prefix, a multiple of the match unit shorter than the prompt;
+ *   - takes a private slot for the request (copy-on-write destination; LRU-evicting an unpinned cached
+ *     state when the pool is full) and pins the cached source until commit;
+ *   - lists one entry per match-unit boundary p in (start_pos, len] in ckpt_slots: a slot to keep the
+ *     state at p, or -1.  Call kda_prefill_chunked with ckpt_interval = the match unit, these slots,
+ *     start_pos, src = private_slot and dst = private_slot, after kda_resume_from_slot(src_slot ->
+ *     private_slot) when src_slot >= 0.
+ * Entries a plan creates become visible to lookups only at kda_prefix_commit (after the GPU work), so a
+ * request planned in the same step never resumes from a state still being written.
+ */
+enum kda_retention { KDA_RETAIN_INTERVAL = 0, KDA_RETAIN_SECOND_HIT = 1 };
+
+typedef struct kda_prefix_index kda_prefix_index;
+
+typedef struct kda_prefix_plan_t {
+    uint64_t plan_id;
+    int32_t src_slot;      /* cached state to resume from, or -1 */
+    int32_t private_slot;  /* the request's own slot */
+    int64_t start_pos;     /* tokens covered by src_slot (0 when src_slot is -1) */
+    int32_t num_ckpts;     /* entries written to ckpt_slots */
+    int32_t reserved;
+} kda_prefix_plan_t;
+
+/* num_slots: pool slots the index manages; match_unit: tokens per hashed block (e.g. 128);
+ * interval: 0, or a multiple of match_unit (interval retention keeps multiples of it and the prompt's last
+ * boundary; second-hit retention keeps seen interval boundaries and the longest seen boundary).  NULL on
+ * invalid arguments. */
+KDA_API kda_prefix_index *kda_prefix_index_create(int32_t num_slots, int32_t match_unit, int32_t policy,
+                                                  int64_t interval);
+KDA_API void kda_prefix_index_destroy(kda_prefix_index *ix);
+/* Slots currently unassigned (-1 for a NULL index). */
+KDA_API int32_t kda_prefix_index_free_slots(kda_prefix_index *ix);
+/* tokens: host [len] int32 token ids.  ckpt_slots: host [ckpt_capacity] int32, receives num_ckpts entries.
+ * KDA_ERR_INVALID_ARG for bad arguments or too small a capacity; KDA_ERR_WORKSPACE when no private slot can
+ * be found (every slot pinned or pending). */
+KDA_API int kda_prefix_plan(kda_prefix_index *ix, const int32_t *tokens, int64_t len, kda_prefix_plan_t *out,
+                            int32_t *ckpt_slots, int32_t ckpt_capacity);
+/* Publish the plan's entries and unpin its source (call once its GPU work has completed). */
+KDA_API int kda_prefix_commit(kda_prefix_index *ix, uint64_t plan_id);
+/* Drop an uncommitted plan: its new entries and its private slot return to the free list. */
+KDA_API int kda_prefix_abort(kda_prefix_index *ix, uint64_t plan_id);
+/* Return a request's private slot (not a cached state) to the free list when the request ends. */
+KDA_API int kda_prefix_release_slot(kda_prefix_index *ix, int32_t slot);
+
 /* Static description of a kda_status value. */
 KDA_API const char *kda_status_string(int status);
 
