@@ -423,9 +423,12 @@ def run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws):
         return {"error": f"device status {int(status.item())}"}
     per_ht = 2 * DK * DV * 2 + 2 * (W - 1) * (2 * DK + DV) * 2 + (3 * DK + DK + DV + DV) * 2 + 2
     gbs = per_ht * DEC_N * H / (ms / 1000.0) / 1e9
+    sha = file_sha("hybrid_linear_attention_decode_gb300/csrc/kda_decode.cu",
+                   "hybrid_linear_attention_decode_gb300/csrc/kda_device.cuh")
     return {"workload": "decode step as above on a bf16 state pool (4096 slots, 4 GiB)",
             "tokens_per_s": DEC_N * ws / (ms / 1000.0), "ms_per_step": ms, "steps": K,
-            "algorithmic_bytes_per_launch": per_ht * DEC_N * H, "achieved_gbs": gbs, "hbm_frac": gbs / hbm_peak}
+            "algorithmic_bytes_per_launch": per_ht * DEC_N * H, "achieved_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+            "traffic": profiled_traffic("kda_decode_bf16", sha)}
 
 
 def prefill_problem(seed: int, lens, chunk: int, interval: int, num_slots: int):
@@ -486,8 +489,9 @@ def run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
 
 
 def run_profile_case(args):
-    """Small case for ncu captures of one kernel: decode on a 768-slot pool (1.5 GiB, larger than L2),
-    batch 64, a fresh slot draw per launch; or one prefill call of the benchmark's prefill workload."""
+    """Small case for ncu captures of one kernel: decode on a 768-slot pool (1.5 GiB fp32 or 0.8 GiB bf16
+    states, larger than L2), batch 64, a fresh slot draw per launch; or one prefill call of the benchmark's
+    prefill workload."""
     import torch
     import hybrid_linear_attention_decode_gb300 as kda
     kda.load_library()
@@ -496,9 +500,10 @@ def run_profile_case(args):
     seed = 2
     wts = ki.layer_weights(seed, H, DK, DV, W)
     prm = kda.LayerParams(torch.from_numpy(wts["conv_w"]).to(dev), torch.from_numpy(wts["norm_w"]).to(dev))
-    if args.profile == "decode":
+    if args.profile in ("decode", "decode_bf16"):
         slots_n = 768
-        pool = kda.StatePool.empty(slots_n, H, DK, DV, W, device=dev)
+        sdt = torch.bfloat16 if args.profile == "decode_bf16" else torch.float32
+        pool = kda.StatePool.empty(slots_n, H, DK, DV, W, device=dev, state_dtype=sdt)
         ki.fill_device_pool(pool.S, pool.conv, seed)
         tok = ki.token_inputs(seed, DEC_N, H, DK, DV)
         d = {k: bf16_dev(v, dev) for k, v in tok.items()}
@@ -513,7 +518,7 @@ def run_profile_case(args):
                                 status, stream)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        print(f"profile case decode: {n} launches")
+        print(f"profile case {args.profile}: {n} launches")
     else:
         pool = kda.StatePool.empty(512, H, DK, DV, W, device=dev)
         r = run_prefill(argparse.Namespace(steps=1, warmup=args.warmup), kda, torch, dev, stream, pool, prm, seed,
@@ -529,7 +534,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_bf16", "prefill"], default=None,
                     help="run a small case of one kernel for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:

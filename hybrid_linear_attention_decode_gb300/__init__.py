@@ -25,9 +25,10 @@ KDA_DEV_BAD_SLOT, KDA_DEV_BAD_SEQLENS, KDA_DEV_BAD_CKPT, KDA_DEV_TIMEOUT = 1, 2,
 
 
 class KdaError(RuntimeError):
-    def __init__(self, rc: int, what: str):
-        super().__init__(f"{what}: {kda_status_string(rc)} (status {rc})")
+    def __init__(self, rc: int, what: str, detail: str = ""):
+        super().__init__(f"{what}: {kda_status_string(rc)} (status {rc})" + (f": {detail}" if detail else ""))
         self.rc = rc
+        self.detail = detail
 
 
 KDA_STATE_FP32, KDA_STATE_BF16 = 0, 1
@@ -79,6 +80,12 @@ def load_library(path: str | None = None):
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_version.restype = ctypes.c_int
+    lib.kda_last_error_string.argtypes = []
+    lib.kda_last_error_string.restype = ctypes.c_char_p
+    lib.kda_check_slots.argtypes = [i64, i32, vp, vp, i32, vp]
+    lib.kda_check_slots.restype = ctypes.c_int
+    lib.kda_selftest_wait_timeout.argtypes = [i64, vp, vp]
+    lib.kda_selftest_wait_timeout.restype = ctypes.c_int
     lib.kda_prefix_index_create.argtypes = [i32, i32, i32, i64]
     lib.kda_prefix_index_create.restype = vp
     lib.kda_prefix_index_destroy.argtypes = [vp]
@@ -126,6 +133,10 @@ class StatePool:
         return StatePool(torch.zeros(num_slots, H, dk, dv, dtype=state_dtype, device=device),
                          torch.zeros(num_slots, H, W - 1, 2 * dk + dv, dtype=torch.bfloat16, device=device))
 
+    @property
+    def num_slots(self) -> int:
+        return int(self.S.shape[0])
+
     def c(self) -> _Pool:
         ns, H, dk, dv = self.S.shape
         if self.S.dtype == torch.float32:
@@ -165,9 +176,46 @@ def kda_prefill_workspace_bytes(pool: StatePool, nseq: int, total_tokens: int, c
     return int(load_library().kda_prefill_workspace_bytes(ctypes.byref(pc), int(nseq), int(total_tokens), int(chunk)))
 
 
-def _check(rc: int, what: str) -> None:
+def kda_last_error_string() -> str:
+    return load_library().kda_last_error_string().decode()
+
+
+def _check(rc: int, what: str, detail: bool = True) -> None:
     if rc != KDA_OK:
-        raise KdaError(rc, what)
+        raise KdaError(rc, what, kda_last_error_string() if detail else "")
+
+
+def _host_i32(x):
+    import numpy as np
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32).reshape(-1))
+
+
+def kda_check_slots(num_slots: int, src_slot, dst_slot, ckpt_slots=None) -> None:
+    """Host check of one call's slot-aliasing contract (kda_check_slots in the C ABI); raises KdaError naming
+    the first violation.  Arrays may be host or device tensors or sequences (device ones are copied)."""
+    s, d, c = _host_i32(src_slot), _host_i32(dst_slot), _host_i32(ckpt_slots)
+    if len(s) != len(d):
+        raise ValueError("src_slot and dst_slot differ in length")
+    vp = ctypes.c_void_p
+    rc = load_library().kda_check_slots(int(num_slots), len(s), s.ctypes.data_as(vp), d.ctypes.data_as(vp),
+                                        0 if c is None else len(c), None if c is None else c.ctypes.data_as(vp))
+    _check(rc, "kda_check_slots")
+
+
+def kda_selftest_wait_timeout(limit_ns: int, dev_status, stream=None) -> None:
+    """Run the bounded-wait check: a wait that never completes gives up after limit_ns and sets
+    KDA_DEV_TIMEOUT in dev_status (int32 [1] on the GPU)."""
+    _check(load_library().kda_selftest_wait_timeout(int(limit_ns), _ptr(dev_status), _stream(stream)),
+           "kda_selftest_wait_timeout")
+
+
+# KDA_CHECK_SLOTS=1: every call checks its slot arrays on the host first (copies them from the device and
+# synchronises; for debugging only).
+_DEBUG_SLOTS = os.environ.get("KDA_CHECK_SLOTS", "0") not in ("", "0")
 
 
 def kda_decode_step(pool: StatePool, params: LayerParams, q, k, v, a, b, z, y, src_slot, dst_slot, dev_status,
@@ -175,6 +223,8 @@ def kda_decode_step(pool: StatePool, params: LayerParams, q, k, v, a, b, z, y, s
     """One fused decode token per request; see include/kda.h.  Tensors: q,k,a [n,H,dk] bf16, v,z,y
     [n,H,dv] bf16, b [n,H] bf16, src_slot/dst_slot [n] int32, dev_status [1] int32 (all on the GPU)."""
     n = int(src_slot.shape[0])
+    if _DEBUG_SLOTS:
+        kda_check_slots(pool.num_slots, src_slot, dst_slot)
     pc, pp = pool.c(), params.c()
     rc = load_library().kda_decode_step(ctypes.byref(pc), ctypes.byref(pp), n, _ptr(q), _ptr(k), _ptr(v), _ptr(a),
                                         _ptr(b), _ptr(z), _ptr(y), _ptr(src_slot), _ptr(dst_slot),
@@ -190,6 +240,8 @@ def kda_prefill_chunked(pool: StatePool, params: LayerParams, cu_seqlens, start_
     kda_prefill_workspace_bytes() bytes."""
     nseq = int(start_pos.shape[0])
     T = int(q.shape[0]) if q is not None else 0
+    if _DEBUG_SLOTS:
+        kda_check_slots(pool.num_slots, src_slot, dst_slot, ckpt_slots if ckpt_interval > 0 else None)
     pc, pp = pool.c(), params.c()
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = load_library().kda_prefill_chunked(
@@ -221,6 +273,8 @@ def kda_prefill_chunked_noalloc(pool: StatePool, params: LayerParams, cu_seqlens
 
 def kda_resume_from_slot(pool: StatePool, src_slot, dst_slot, dev_status, stream=None) -> None:
     """Copy-on-write: slot dst_slot[i] receives a bit-exact copy of slot src_slot[i] (int32 [n])."""
+    if _DEBUG_SLOTS:
+        kda_check_slots(pool.num_slots, src_slot, dst_slot)
     pc = pool.c()
     rc = load_library().kda_resume_from_slot(ctypes.byref(pc), int(src_slot.shape[0]), _ptr(src_slot),
                                              _ptr(dst_slot), _ptr(dev_status), _stream(stream))
@@ -273,15 +327,15 @@ class PrefixIndex:
         out = _PrefixPlan()
         rc = self._lib.kda_prefix_plan(self._h, t.ctypes.data_as(ctypes.c_void_p), len(t), ctypes.byref(out),
                                        ck.ctypes.data_as(ctypes.c_void_p), cap)
-        _check(rc, "kda_prefix_plan")
+        _check(rc, "kda_prefix_plan", detail=False)
         return PrefixPlan(int(out.plan_id), int(out.src_slot), int(out.private_slot), int(out.start_pos),
                           [int(x) for x in ck[:out.num_ckpts]])
 
     def commit(self, plan: PrefixPlan) -> None:
-        _check(self._lib.kda_prefix_commit(self._h, plan.plan_id), "kda_prefix_commit")
+        _check(self._lib.kda_prefix_commit(self._h, plan.plan_id), "kda_prefix_commit", detail=False)
 
     def abort(self, plan: PrefixPlan) -> None:
-        _check(self._lib.kda_prefix_abort(self._h, plan.plan_id), "kda_prefix_abort")
+        _check(self._lib.kda_prefix_abort(self._h, plan.plan_id), "kda_prefix_abort", detail=False)
 
     def release_slot(self, slot: int) -> None:
-        _check(self._lib.kda_prefix_release_slot(self._h, int(slot)), "kda_prefix_release_slot")
+        _check(self._lib.kda_prefix_release_slot(self._h, int(slot)), "kda_prefix_release_slot", detail=False)

@@ -320,20 +320,20 @@ static int launch_decode_t(const DecodeArgs &a, cudaStream_t st) {
     auto kern = kda_decode_kernel<DK, DV, NBUF, SBF>;
     static int occ_cache[64] = {0};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_result("decode: cudaGetDevice");
     if (occ_cache[dev] == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return KDA_ERR_CUDA;
+            return launch_result("decode: cudaFuncSetAttribute");
         int occ = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::NT, C::SMEM) != cudaSuccess || occ < 1)
-            return KDA_ERR_CUDA;
+            return fail(KDA_ERR_CUDA, "decode: the kernel cannot be resident on this device");
         occ_cache[dev] = occ;
     }
     const int items = a.n * a.H;
     const int cap = current_device_sms() * occ_cache[dev];
     const int grid = items < cap ? items : cap;
     kern<<<grid, C::NT, C::SMEM, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return launch_result("kda_decode_kernel launch");
 }
 
 bool decode_supported(int dk, int dv, int W) {

@@ -78,13 +78,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Waits for the phase of `bar` with the given parity; gives up after kWaitLimitNs and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Waits for the phase of `bar` with the given parity; gives up after limit_ns and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

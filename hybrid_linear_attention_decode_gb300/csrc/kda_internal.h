@@ -70,4 +70,11 @@ int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st);
 // Streaming multiprocessors of the current device (cached per device).
 int current_device_sms();
 
+// Per-host-thread description of the most recent failure, read by kda_last_error_string().
+// fail() records `what` and returns `code`; clear_error() runs at the start of every entry point.
+int fail(int code, const char *what);
+void clear_error();
+// KDA_OK if the launches just issued were accepted; else KDA_ERR_CUDA with "<what>: <CUDA error>" recorded.
+int launch_result(const char *what);
+
 }  // namespace kda

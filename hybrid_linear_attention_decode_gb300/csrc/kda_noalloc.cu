@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/kda.h"
+#include "kda_internal.h"
 
 namespace {
 
@@ -44,11 +45,13 @@ extern "C" KDA_API int kda_prefill_chunked_noalloc(
     const int64_t *start_pos, const int32_t *src_slot, const int32_t *dst_slot, int32_t chunk, int64_t ckpt_interval,
     const int32_t *ckpt_offsets, const int32_t *ckpt_slots, const uint16_t *q, const uint16_t *k, const uint16_t *v,
     const uint16_t *a, const uint16_t *b, const uint16_t *z, uint16_t *y, int32_t *dev_status, kda_stream_t stream) {
+    kda::clear_error();
     // Reject problems whose workspace does not fit the fixed scratch before touching the device.
     const size_t need = kda_prefill_workspace_bytes(pool, nseq, total_tokens, chunk);
-    if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+    if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES)
+        return kda::fail(KDA_ERR_WORKSPACE, "prefill_noalloc: workspace larger than the static scratch");
     void *scratch = scratch_on_current_device();
-    if (!scratch) return KDA_ERR_CUDA;
+    if (!scratch) return kda::fail(KDA_ERR_CUDA, "prefill_noalloc: cudaGetSymbolAddress of the scratch failed");
     // Every field of the workspace is written before it is read, so the contents left by an earlier
     // call need no clearing.
     return kda_prefill_chunked(pool, prm, nseq, total_tokens, cu_seqlens, start_pos, src_slot, dst_slot, chunk,

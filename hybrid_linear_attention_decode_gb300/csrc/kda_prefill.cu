@@ -1217,16 +1217,16 @@ static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     const tc::Layout2 L2 = tc::make_layout2(a.H, a.nseq, a.total_tokens);
     static int attr_done[64] = {0};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_result("prefill: cudaGetDevice");
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(tc::prefill_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tc::I_SMEM) != cudaSuccess ||
             cudaFuncSetAttribute(tc::prefill_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tc::S_SMEM) != cudaSuccess)
-            return KDA_ERR_CUDA;
+            return launch_result("prefill: cudaFuncSetAttribute");
         attr_done[dev] = 1;
     }
-    if (L2.maxc > 0x7fffffffLL || a.H > 65535) return KDA_ERR_INVALID_ARG;
+    if (L2.maxc > 0x7fffffffLL || a.H > 65535) return fail(KDA_ERR_INVALID_ARG, "prefill: grid too large");
     prefill_table_kernel<<<1, kMaxSeqThreads, 0, st>>>(a, tc::as_layout(L2));
     if (a.total_tokens > 0) {
         dim3 gi((unsigned)L2.maxc, a.H);
@@ -1234,7 +1234,7 @@ static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     }
     dim3 gs(a.nseq, a.H);
     tc::prefill_state_tc_kernel<<<gs, tc::NT, tc::S_SMEM, st>>>(a, L2);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return launch_result("prefill (tensor-core path) launch");
 }
 
 int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st) {
@@ -1246,17 +1246,17 @@ int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st) {
     const size_t smem_state = sizeof(float) * (dk * DVT + 3 * C * dk + C * C + 2 * C * DVT + dk);
     static int attr_done[64] = {0};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_result("prefill: cudaGetDevice");
     if (!attr_done[dev]) {
         const int max_smem = 227 * 1024;
         if (cudaFuncSetAttribute(prefill_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
                 cudaSuccess ||
             cudaFuncSetAttribute(prefill_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
                 cudaSuccess)
-            return KDA_ERR_CUDA;
+            return launch_result("prefill: cudaFuncSetAttribute");
         attr_done[dev] = 1;
     }
-    if (L.maxc > 0x7fffffffLL || a.H > 65535) return KDA_ERR_INVALID_ARG;
+    if (L.maxc > 0x7fffffffLL || a.H > 65535) return fail(KDA_ERR_INVALID_ARG, "prefill: grid too large");
     prefill_table_kernel<<<1, kMaxSeqThreads, 0, st>>>(a, L);
     if (a.total_tokens > 0) {
         dim3 gi((unsigned)L.maxc, a.H);
@@ -1268,7 +1268,7 @@ int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st) {
         dim3 go((unsigned)L.maxc, a.H);
         prefill_out_kernel<<<go, kThreads, 0, st>>>(a, L, dv);
     }
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return launch_result("prefill launch");
 }
 
 }  // namespace kda

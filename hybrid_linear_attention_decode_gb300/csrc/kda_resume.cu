@@ -41,9 +41,9 @@ __global__ void __launch_bounds__(kResumeThreads) kda_resume_kernel(const Resume
 
 int launch_resume(const ResumeArgs &a, cudaStream_t st) {
     const long long blocks = (long long)a.n * a.H;
-    if (blocks > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (blocks > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "resume: n * H too large");
     kda_resume_kernel<<<(unsigned)blocks, kResumeThreads, 0, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return launch_result("kda_resume_kernel launch");
 }
 
 }  // namespace kda

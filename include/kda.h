@@ -239,6 +239,33 @@ KDA_API int kda_prefix_release_slot(kda_prefix_index *ix, int32_t slot);
 /* Static description of a kda_status value. */
 KDA_API const char *kda_status_string(int status);
 
+/* What the last failing call of the calling host thread rejected ("decode: q, k, v, a and z must be
+ * 16-byte aligned", "prefill launch: <CUDA error text>", ...), or "" when the last call of the thread to
+ * kda_decode_step, kda_prefill_chunked(_noalloc), kda_resume_from_slot or kda_check_slots succeeded.  The
+ * string belongs to the library and stays valid until the thread's next such call.  Library-side record
+ * only; nothing in the pages defines it. */
+KDA_API const char *kda_last_error_string(void);
+
+/*
+ * Debug check of one call's slot-aliasing contract, on HOST copies of its slot arrays.  The kernels rely
+ * on it but do not check it; it is the host-side form of "same-step reuse is deferred" ("A Preview of
+ * Production-Scale Kimi K3 Support on vLLM", section "The Hardest Part: Prefix Caching for KDA").
+ *   - every dst_slot[i] in [0, num_slots), every src_slot[i] and ckpt_slots[j] in [-1, num_slots);
+ *   - no slot is written twice: the dst slots and the non-negative checkpoint slots are distinct;
+ *   - a src slot is written by nobody but its own item (src_slot[i] == dst_slot[i] is in place).
+ * Decode: n_ckpt = 0.  Resume: src/dst as passed.  Prefill: its ckpt_slots table.  KDA_OK, or
+ * KDA_ERR_INVALID_ARG with kda_last_error_string() naming the first violation.  O((n + n_ckpt) log), no
+ * device access.
+ */
+KDA_API int kda_check_slots(int64_t num_slots, int32_t n, const int32_t *src_slot, const int32_t *dst_slot,
+                            int32_t n_ckpt, const int32_t *ckpt_slots);
+
+/* Failure-detection check of the bounded waits every kernel uses (no counterpart in the pages): launches
+ * one CTA whose mbarrier wait can never complete; after limit_ns (clamped to [1 ms, 2 s]) of %globaltimer it
+ * gives up, ORs KDA_DEV_TIMEOUT into *dev_status (device int32) and returns.  No fault, no trap: the context
+ * stays usable.  Asynchronous on `stream`. */
+KDA_API int kda_selftest_wait_timeout(int64_t limit_ns, int32_t *dev_status, kda_stream_t stream);
+
 /* Library version, for the loader's sanity check. */
 KDA_API int kda_version(void);
 

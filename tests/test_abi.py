@@ -99,3 +99,48 @@ def test_noalloc_scratch_size_matches_header():
     src = open(os.path.join(ROOT, "include", "kda.h")).read()
     m = re.search(r"#define KDA_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", src)
     assert m and int(m.group(1)) << int(m.group(2)) == kda.NOALLOC_SCRATCH_BYTES
+
+
+def test_last_error_names_the_rejected_argument(lib):
+    import hybrid_linear_attention_decode_gb300 as kda
+    prm = kda._Params(ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000), 1e-6, 1e-6, 1.0, 1)
+    mis = kda._Pool(2, 128, 128, 4, 0, 0, 8, ctypes.c_void_p(0x1004), ctypes.c_void_p(0x2000))
+    assert lib.kda_decode_step(ctypes.byref(mis), ctypes.byref(prm), 1, *([None] * 11)) == kda.KDA_ERR_INVALID_ARG
+    assert "16-byte aligned" in kda.kda_last_error_string()
+    bad = kda._Pool(2, 96, 128, 4, 0, 0, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
+    assert lib.kda_decode_step(ctypes.byref(bad), ctypes.byref(prm), 1, *([None] * 11)) == \
+        kda.KDA_ERR_UNSUPPORTED_SHAPE
+    assert "not compiled in" in kda.kda_last_error_string()
+    pool = kda._Pool(2, 128, 128, 4, 0, 0, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
+    assert lib.kda_resume_from_slot(ctypes.byref(pool), 0, None, None, None, None) == kda.KDA_OK
+    assert kda.kda_last_error_string() == ""  # a successful call clears it
+    # the interval must be a multiple of the chunk
+    rc = lib.kda_prefill_chunked(ctypes.byref(pool), ctypes.byref(prm), 1, 0, *([None] * 4), 64, 96,
+                                 *([None] * 9), None, 0, None, None)
+    assert rc == kda.KDA_ERR_INVALID_ARG and "multiple of the chunk" in kda.kda_last_error_string()
+    with pytest.raises(kda.KdaError) as e:
+        kda._check(rc, "kda_prefill_chunked")
+    assert "multiple of the chunk" in str(e.value)
+
+
+def test_check_slots_enforces_the_aliasing_contract(lib):
+    import hybrid_linear_attention_decode_gb300 as kda
+    ok = kda.kda_check_slots
+    ok(8, [0, 1, 2], [0, 1, 2])                 # in place
+    ok(8, [-1, -1], [3, 4])                     # fresh requests
+    ok(8, [0, 1], [5, 6], [7, -1, 2])           # prefill with checkpoints; -1 skips
+    ok(8, [], [])
+    cases = [
+        ((8, [0, 1], [2, 2]), "written twice"),            # duplicate dst
+        ((8, [0, 1], [1, 2]), "written by another"),       # src of item 1 is the dst of item 0
+        ((8, [0], [1], [0]), "written by another"),        # src is a checkpoint slot
+        ((8, [0], [0], [0]), "written twice"),             # in place, but also a checkpoint
+        ((8, [0], [1], [1]), "written twice"),             # checkpoint equals a dst
+        ((8, [0], [8]), "outside"),
+        ((8, [-2], [1]), "outside"),
+        ((8, [0], [1], [9]), "outside"),
+    ]
+    for args, words in cases:
+        with pytest.raises(kda.KdaError) as e:
+            ok(*args)
+        assert e.value.rc == kda.KDA_ERR_INVALID_ARG and words in str(e.value), (args, str(e.value))
