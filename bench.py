@@ -355,6 +355,9 @@ def run_gpu(args):
     # ---- the same decode step on a bf16 state pool
     decode_bf16 = run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws)
 
+    # ---- speculative verification: 5 tokens per request, every position kept
+    decode_multi = run_decode_multi(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
+
     # ---- chunked prefill workload
     prefill = run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
 
@@ -375,6 +378,7 @@ def run_gpu(args):
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": K,
             "decode_bf16_state": decode_bf16,
+            "decode_multi_verify": decode_multi,
             "prefill": prefill}
     if rank == 0:
         if ws == 1 and not args.no_cpu_baseline:
@@ -383,6 +387,60 @@ def run_gpu(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+MULTI_L = 5  # verify step: 4 draft tokens + 1
+
+
+def run_decode_multi(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
+    """Speculative verification on the decode workload's fp32 pool: 64 requests x 5 tokens in one launch,
+    the state after every position kept in its own slot; each step draws 64 + 320 fresh distinct slots."""
+    L = MULTI_L
+    tok = ki.token_inputs(seed + 3, DEC_N * L, H, DK, DV)
+    d = {k: bf16_dev(v, dev) for k, v in tok.items()}
+    y = torch.empty(DEC_N * L, H, DV, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    K, Wm = max(3, min(args.steps, 500)), args.warmup
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed + 3)
+    draw = torch.rand(K + Wm, DEC_SLOTS, device=dev, generator=g).argsort(dim=1)[:, :DEC_N * (L + 1)]
+    draw = draw.to(torch.int32)
+    src = draw[:, :DEC_N].contiguous()
+    dst = draw[:, DEC_N:].contiguous()
+
+    def step(i, st=stream):
+        kda.kda_decode_multi(pool, prm, L, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y, src[i], dst[i], status,
+                             st)
+
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(K):
+            step(Wm + i, None)
+    graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws) / K
+    del graph
+    if int(status.item()) != 0:
+        return {"error": f"device status {int(status.item())}"}
+    # per (request, head): one state + window read, L state + window writes, L tokens of q,k,v,a,z,y,b
+    per_item = (1 + L) * DK * DV * 4 + (1 + L) * (W - 1) * (2 * DK + DV) * 2 + L * ((3 * DK + DK + DV + DV) * 2 + 2)
+    gbs = per_item * DEC_N * H / (ms / 1000.0) / 1e9
+    return {"workload": "verify step: 64 requests x 5 tokens (4 draft + 1), H=32, dk=dv=128, fp32 pool of 4096 "
+                        "slots, the state after every position kept in its own slot, fresh random slots per step",
+            "tokens_per_s": DEC_N * L * ws / (ms / 1000.0), "ms_per_step": ms, "steps": K,
+            "algorithmic_bytes_per_launch": per_item * DEC_N * H, "achieved_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+            "traffic": profiled_traffic("kda_decode_multi", file_sha(
+                "hybrid_linear_attention_decode_gb300/csrc/kda_decode_multi.cu",
+                "hybrid_linear_attention_decode_gb300/csrc/kda_device.cuh"))}
 
 
 def run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws):
@@ -490,8 +548,8 @@ def run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
 
 def run_profile_case(args):
     """Small case for ncu captures of one kernel: decode on a 768-slot pool (1.5 GiB fp32 or 0.8 GiB bf16
-    states, larger than L2), batch 64, a fresh slot draw per launch; or one prefill call of the benchmark's
-    prefill workload."""
+    states, larger than L2), batch 64, a fresh slot draw per launch; the 5-token verify step on the same
+    pool; or one prefill call of the benchmark's prefill workload."""
     import torch
     import hybrid_linear_attention_decode_gb300 as kda
     kda.load_library()
@@ -519,6 +577,24 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         print(f"profile case {args.profile}: {n} launches")
+    elif args.profile == "decode_multi":
+        slots_n, L = 768, MULTI_L
+        pool = kda.StatePool.empty(slots_n, H, DK, DV, W, device=dev)
+        ki.fill_device_pool(pool.S, pool.conv, seed)
+        tok = ki.token_inputs(seed, DEC_N * L, H, DK, DV)
+        d = {k: bf16_dev(v, dev) for k, v in tok.items()}
+        y = torch.empty(DEC_N * L, H, DV, dtype=torch.bfloat16, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        n = args.warmup + args.steps
+        draw = torch.rand(n, slots_n, device=dev, generator=g).argsort(dim=1)[:, :DEC_N * (L + 1)].to(torch.int32)
+        for i in range(n):
+            kda.kda_decode_multi(pool, prm, L, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y,
+                                 draw[i, :DEC_N].contiguous(), draw[i, DEC_N:].contiguous(), status, stream)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        print(f"profile case decode_multi: {n} launches")
     else:
         pool = kda.StatePool.empty(512, H, DK, DV, W, device=dev)
         r = run_prefill(argparse.Namespace(steps=1, warmup=args.warmup), kda, torch, dev, stream, pool, prm, seed,
@@ -534,7 +610,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode_bf16", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_bf16", "decode_multi", "prefill"], default=None,
                     help="run a small case of one kernel for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -4,7 +4,7 @@ Argument marshalling only: every step of the path runs in the CUDA kernels behin
 ``include/kda.h``.  PyTorch provides device memory and streams.  There is no fallback: if the library
 is missing the import of an entry point raises.
 
-Entry points (same names as the C ABI): ``kda_decode_step``, ``kda_prefill_chunked``,
+Entry points (same names as the C ABI): ``kda_decode_step``, ``kda_decode_multi``, ``kda_prefill_chunked``,
 ``kda_resume_from_slot``, ``kda_prefill_workspace_bytes``, ``kda_checkpoint_count``,
 ``kda_status_string``; the host prefix index ``kda_prefix_*`` through :class:`PrefixIndex`.
 """
@@ -65,6 +65,8 @@ def load_library(path: str | None = None):
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     lib.kda_decode_step.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Params), i32] + [vp] * 11
     lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_decode_multi.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Params), i32, i32] + [vp] * 11
+    lib.kda_decode_multi.restype = ctypes.c_int
     lib.kda_checkpoint_count.argtypes = [i64, i64, i64]
     lib.kda_checkpoint_count.restype = i64
     lib.kda_prefill_workspace_bytes.argtypes = [ctypes.POINTER(_Pool), i32, i64, i32]
@@ -230,6 +232,31 @@ def kda_decode_step(pool: StatePool, params: LayerParams, q, k, v, a, b, z, y, s
                                         _ptr(b), _ptr(z), _ptr(y), _ptr(src_slot), _ptr(dst_slot),
                                         _ptr(dev_status), _stream(stream))
     _check(rc, "kda_decode_step")
+
+
+DECODE_MULTI_MAX_L = 8  # KDA_DECODE_MULTI_MAX_L in kda.h
+
+
+def kda_decode_multi(pool: StatePool, params: LayerParams, L: int, q, k, v, a, b, z, y, src_slot, dst_slots,
+                     dev_status, stream=None) -> None:
+    """L consecutive decode tokens per request with per-position state retention (speculative verification);
+    see include/kda.h.  q,k,a [n*L,H,dk], v,z,y [n*L,H,dv], b [n*L,H] bf16 (row r*L+j = token j of request r);
+    src_slot [n] int32; dst_slots [n*L] int32 (-1 = position not kept)."""
+    n = int(src_slot.shape[0])
+    if _DEBUG_SLOTS:
+        kept = _host_i32(dst_slots)
+        kda_check_slots(pool.num_slots, [], [], kept)
+        src_h = _host_i32(src_slot)
+        for r, s_ in enumerate(src_h):
+            others = set(kept[:r * L].tolist()) | set(kept[(r + 1) * L:].tolist())
+            if s_ >= 0 and int(s_) in others:
+                raise KdaError(KDA_ERR_INVALID_ARG, "kda_decode_multi",
+                               f"src_slot[{r}] = {s_} is kept by another request")
+    pc, pp = pool.c(), params.c()
+    rc = load_library().kda_decode_multi(ctypes.byref(pc), ctypes.byref(pp), n, int(L), _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(a), _ptr(b), _ptr(z), _ptr(y), _ptr(src_slot), _ptr(dst_slots),
+                                         _ptr(dev_status), _stream(stream))
+    _check(rc, "kda_decode_multi")
 
 
 def kda_prefill_chunked(pool: StatePool, params: LayerParams, cu_seqlens, start_pos, src_slot, dst_slot, chunk: int,

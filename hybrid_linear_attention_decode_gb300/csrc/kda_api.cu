@@ -181,6 +181,48 @@ int kda_decode_step(const kda_pool *pool, const kda_params *prm, int32_t n, cons
     return launch_decode(d, pool->dk, pool->dv, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kda_decode_multi(const kda_pool *pool, const kda_params *prm, int32_t n, int32_t L, const uint16_t *q,
+                     const uint16_t *k, const uint16_t *v, const uint16_t *a, const uint16_t *b, const uint16_t *z,
+                     uint16_t *y, const int32_t *src_slot, const int32_t *dst_slots, int32_t *dev_status,
+                     kda_stream_t stream) {
+    clear_error();
+    int rc = check_pool(pool, prm);
+    if (rc != KDA_OK) return rc;
+    if (!prm) return fail(KDA_ERR_INVALID_ARG, "decode_multi: params is NULL");
+    if (n < 0) return fail(KDA_ERR_INVALID_ARG, "decode_multi: n < 0");
+    if (L < 1 || L > KDA_DECODE_MULTI_MAX_L)
+        return fail(KDA_ERR_INVALID_ARG, "decode_multi: L outside [1, KDA_DECODE_MULTI_MAX_L]");
+    if (!decode_supported(pool->dk, pool->dv, pool->conv_w))
+        return fail(KDA_ERR_UNSUPPORTED_SHAPE, "decode_multi: (dk, dv, conv_w) not compiled in");
+    if (n == 0) return KDA_OK;
+    if ((int64_t)n * L * pool->H > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "decode_multi: n * L * H too large");
+    if (!q || !k || !v || !a || !b || !y || !src_slot || !dst_slots)
+        return fail(KDA_ERR_INVALID_ARG, "decode_multi: a required pointer is NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || (z && !aligned16(z)))
+        return fail(KDA_ERR_INVALID_ARG, "decode_multi: q, k, v, a and z must be 16-byte aligned");
+    if (!aligned2(b) || !aligned2(y) || !aligned4(src_slot) || !aligned4(dst_slots) ||
+        (dev_status && !aligned4(dev_status)))
+        return fail(KDA_ERR_INVALID_ARG, "decode_multi: b, y, slot arrays or status misaligned");
+    DecodeArgs d;
+    d.S = pool->S;
+    d.state_bf16 = pool->state_dtype == KDA_STATE_BF16;
+    d.conv = pool->conv;
+    d.num_slots = pool->num_slots;
+    d.H = pool->H;
+    d.n = n;
+    d.conv_w = prm->conv_weight;
+    d.norm_w = prm->norm_weight;
+    d.l2_eps = prm->l2_eps;
+    d.rms_eps = prm->rms_eps;
+    d.scale = prm->scale;
+    d.silu = prm->conv_silu;
+    d.q = q; d.k = k; d.v = v; d.a = a; d.b = b; d.z = z; d.y = y;
+    d.src = src_slot;
+    d.dst = dst_slots;
+    d.status = dev_status;
+    return launch_decode_multi(d, pool->dk, pool->dv, L, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t kda_prefill_workspace_bytes(const kda_pool *pool, int32_t nseq, int64_t total_tokens, int32_t chunk) {
     if (!pool || nseq < 0 || total_tokens < 0 || pool->H <= 0) return 0;
     if (!prefill_supported(pool->dk, pool->dv, pool->conv_w, chunk)) return 0;

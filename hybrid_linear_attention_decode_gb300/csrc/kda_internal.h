@@ -60,6 +60,8 @@ struct PrefillArgs {
 
 bool decode_supported(int dk, int dv, int W);
 int launch_decode(const DecodeArgs &a, int dk, int dv, cudaStream_t st);
+// L tokens per request; a.dst is the [n*L] table of kept positions (-1 = not kept).
+int launch_decode_multi(const DecodeArgs &a, int dk, int dv, int L, cudaStream_t st);
 
 int launch_resume(const ResumeArgs &a, cudaStream_t st);
 

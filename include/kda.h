@@ -110,6 +110,33 @@ KDA_API int kda_decode_step(const kda_pool *pool, const kda_params *prm, int32_t
                     const uint16_t *v, const uint16_t *a, const uint16_t *b, const uint16_t *z, uint16_t *y,
                     const int32_t *src_slot, const int32_t *dst_slot, int32_t *dev_status, kda_stream_t stream);
 
+/* Most tokens per request that one kda_decode_multi call takes. */
+#define KDA_DECODE_MULTI_MAX_L 8
+
+/*
+ * L consecutive decode tokens for each of n requests in one launch, keeping the state after every position
+ * on request: the verification step of speculative decoding ("vLLM Kimi K3 Support", section "Speculative
+ * Decoding with DSpark": several tokens accepted per step; "moonshotai/Kimi-K3" recipe:
+ * num_speculative_tokens 4, i.e. L = 5 with the bonus position).  The pages do not say how a recurrent state
+ * is rolled back after a rejection; here the caller keeps the state at each position it may resume from
+ * (per-position retention) and continues from the slot of the last accepted position.
+ *   q, k, a   device [n*L][H][dk] bf16   v, z, y  device [n*L][H][dv] bf16   b  device [n*L][H] bf16
+ *             (row r*L + j holds token j of request r; z may be NULL)
+ *   src_slot  device [n] int32: state before token 0; -1 = fresh request
+ *   dst_slots device [n*L] int32: the state and conv window after token j of request r go to slot
+ *             dst_slots[r*L + j]; -1 = not kept.  The tokens are processed in order with the state held in
+ *             fp32 between them, whatever is kept.
+ *   dev_status device int32, OR-ed with KDA_DEV_* bits.
+ * Each token's arithmetic is that of kda_decode_step, so L = 1 with dst_slots = dst_slot reproduces it bit
+ * for bit.  Aliasing: the non-negative dst_slots of one call are distinct; a request's src may be one of its
+ * own dst_slots, never another request's.  A request with a bad slot index gets y = 0 for all L tokens and
+ * no state write.  1 <= L <= KDA_DECODE_MULTI_MAX_L; shapes as kda_decode_step.
+ */
+KDA_API int kda_decode_multi(const kda_pool *pool, const kda_params *prm, int32_t n, int32_t L, const uint16_t *q,
+                             const uint16_t *k, const uint16_t *v, const uint16_t *a, const uint16_t *b,
+                             const uint16_t *z, uint16_t *y, const int32_t *src_slot, const int32_t *dst_slots,
+                             int32_t *dev_status, kda_stream_t stream);
+
 /*
  * Checkpoint boundaries of one sequence: the prefix lengths p with p % interval == 0 and
  * start_pos < p <= start_pos + len ("vLLM Kimi K3 Support", section "Agentic Cache Retention Policies":

@@ -16,7 +16,9 @@ gcc, marshals numpy arrays, and states the slot-pool semantics of the three oper
   Policies"): the j-th boundary of sequence n goes to ``ckpt_slots[ckpt_offsets[n] + j]`` unless that
   entry is -1;
 * resume ("The Hardest Part: Prefix Caching for KDA", copy-on-write): slot ``dst[n]`` receives a copy
-  of slot ``src[n]``.
+  of slot ``src[n]``;
+* multi-token decode ("vLLM Kimi K3 Support", section "Speculative Decoding with DSpark"): L tokens per
+  request in order, the state after token j kept in slot ``dst_slots[r*L + j]`` unless it is -1.
 
 Parity unpinned by the pages: they print no worked numeric example; every pin in the test suite comes
 from algebra (closed forms, invariants, brute force, exact rational arithmetic).
@@ -208,6 +210,31 @@ def decode_pool(cfg: Cfg, pool_S, pool_conv, src_slot, dst_slot, q, k, v, a, b, 
         out_S[d] = _store(r["S"][n], state_bf16)
         out_C[d] = r["conv"][n]
     return dict(pool_S=out_S, pool_conv=out_C, o=r["o"], y=r["y"])
+
+
+def decode_multi_pool(cfg: Cfg, pool_S, pool_conv, L: int, src_slot, dst_slots, q, k, v, a, b, z, conv_w, norm_w,
+                      state_bf16: bool = False) -> dict:
+    """L consecutive decode tokens per request with per-position retention (speculative verification).
+
+    Token j of request r is row r*L + j of q..z.  The recurrence runs through the L tokens of each request
+    from slot src_slot[r] (zeros when -1); the state and window after token j are written to slot
+    dst_slots[r*L + j] unless it is -1 (the rollback reading: every position the caller may resume from is
+    kept).  Returns the fp64 pools after the call, o and y [n*L,H,dv], and the per-position states.
+    """
+    n = len(src_slot)
+    dst = np.asarray(dst_slots, dtype=np.int64).reshape(n, L)
+    S0, C0 = _gather(pool_S, pool_conv, src_slot)
+    r = forward(cfg, np.arange(n + 1) * L, np.zeros(n, dtype=np.int64), q, k, v, a, b, z, conv_w, norm_w, S0, C0,
+                interval=1)
+    assert len(r["ckpt_pos"]) == n * L  # interval 1: a boundary after every token
+    out_S = np.array(pool_S, dtype=np.float64, copy=True)
+    out_C = np.array(pool_conv, dtype=np.float64, copy=True)
+    for i in range(n * L):
+        d = dst[i // L, i % L]
+        if d >= 0:
+            out_S[d] = _store(r["ckpt_S"][i], state_bf16)
+            out_C[d] = r["ckpt_conv"][i]
+    return dict(pool_S=out_S, pool_conv=out_C, o=r["o"], y=r["y"], pos_S=r["ckpt_S"], pos_conv=r["ckpt_conv"])
 
 
 def prefill_pool(cfg: Cfg, pool_S, pool_conv, cu_seqlens, start_pos, src_slot, dst_slot, interval,

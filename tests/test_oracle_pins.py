@@ -379,3 +379,50 @@ def test_bf16_pool_rounding_is_nearest_even():
     np.testing.assert_array_equal(oracle.round_to_bf16(x), want)
     vals = ki.bf16_bits_to_f64(ki.f32_to_bf16_bits(RNG.standard_normal(1000).astype(np.float32)))
     np.testing.assert_array_equal(oracle.round_to_bf16(vals), vals)
+
+
+def test_multi_token_decode_equals_chained_single_steps():
+    """The multi-token decode helper (per-position retention) against L single-token oracle steps chained
+    through the pool: outputs, every kept state and window bit for bit; positions marked -1 write nothing;
+    a request whose src is also its last kept slot updates in place."""
+    H, dk, dv, L, n, slots = 2, 4, 3, 4, 3, 16
+    cfg = oracle.Cfg(H=H, dk=dk, dv=dv)
+    rng = np.random.default_rng(77)
+    Cc = 2 * dk + dv
+    pool_S = 0.3 * rng.standard_normal((slots, H, dk, dv))
+    pool_C = rng.standard_normal((slots, H, 3, Cc))
+    tok = dict(q=rng.standard_normal((n * L, H, dk)), k=rng.standard_normal((n * L, H, dk)),
+               v=rng.standard_normal((n * L, H, dv)), a=rng.standard_normal((n * L, H, dk)) + 3.0,
+               b=rng.standard_normal((n * L, H)), z=rng.standard_normal((n * L, H, dv)))
+    conv_w = rng.standard_normal((H, Cc, 4)) / 2.0
+    norm_w = 1 + 0.1 * rng.standard_normal(dv)
+    src = [3, -1, 9]
+    dst = [[4, 5, -1, 6], [7, -1, -1, 8], [10, 11, 12, 9]]
+    r = oracle.decode_multi_pool(cfg, pool_S, pool_C, L, src, np.array(dst).reshape(-1), tok["q"], tok["k"],
+                                 tok["v"], tok["a"], tok["b"], tok["z"], conv_w, norm_w)
+    scratch = [13, 14, 15]  # chain the single steps through spare slots
+    S, C = pool_S.copy(), pool_C.copy()
+    S[scratch] = 0.0
+    C[scratch] = 0.0
+    cur = list(src)
+    for j in range(L):
+        rows = [i * L + j for i in range(n)]
+        step = oracle.decode_pool(cfg, S, C, cur, scratch, *(tok[x][rows] for x in ("q", "k", "v", "a", "b", "z")),
+                                  conv_w, norm_w)
+        S, C = step["pool_S"], step["pool_conv"]
+        np.testing.assert_array_equal(r["y"][rows], step["y"])
+        for i in range(n):
+            np.testing.assert_array_equal(r["pos_S"][i * L + j], S[scratch[i]])
+            if dst[i][j] >= 0:
+                np.testing.assert_array_equal(r["pool_S"][dst[i][j]], S[scratch[i]])
+                np.testing.assert_array_equal(r["pool_conv"][dst[i][j]], C[scratch[i]])
+        cur = list(scratch)
+    kept = {d for row in dst for d in row if d >= 0}
+    for s_ in range(slots):
+        if s_ not in kept:
+            np.testing.assert_array_equal(r["pool_S"][s_], pool_S[s_])
+    # a bf16 pool stores the rounding of the fp64 chain, which itself is never rounded between tokens
+    rb = oracle.decode_multi_pool(cfg, pool_S, pool_C, L, src, np.array(dst).reshape(-1), tok["q"], tok["k"],
+                                  tok["v"], tok["a"], tok["b"], tok["z"], conv_w, norm_w, state_bf16=True)
+    np.testing.assert_array_equal(rb["y"], r["y"])
+    np.testing.assert_array_equal(rb["pool_S"][8], oracle.round_to_bf16(r["pool_S"][8]))
