@@ -20,7 +20,10 @@
 //   3. state:  one CTA per (sequence, head, dv tile), sequential over the sequence's chunks: U, O and the
 //              state chain in fp32; checkpoint states written at every boundary, the final one to dst;
 //   4. out:    gated RMSNorm of O into the bf16 output.
+#include <cuda.h>  // CUtensorMap; the encoder is looked up at run time, so nothing links the driver library
+
 #include <algorithm>
+#include <atomic>
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -511,7 +514,8 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 }
 
 // Intra-chunk kernel smem (bytes, from a 1024-aligned base), by phase:
-//   P0-P1  [0,32K) q^ fp32 | [32K,64K) k^ fp32 | [64K,96K) G fp32 | [96K,128K) V^T tf32 tile | [128K,180K) raw rows
+//   P0-P1  [0,32K) q^ fp32 | [32K,64K) k^ fp32 | [64K,96K) G fp32 (decay logits staged in its first 16K) |
+//          [96K,128K) V^T tf32 tile | [128K,180K) raw rows
 //   P2     [128K,160K) [K+;Q+] bf16 tile | [160K,176K) K- bf16 tile
 //   P3-P4  [0,8K) Qk staging, then [0,16K) Inv fp32 | [128K,145K) A fp32 (row stride 68) | [160K,176K) block temps,
 //          then T tf32
@@ -529,6 +533,20 @@ static_assert(I_A + CH * AST * 4 <= I_QKS_SLOW && I_QKS_SLOW + CH * CH * 2 <= I_
 static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
 
 constexpr int NTI = 512;  // intra kernel threads
+constexpr int RAW_PART = RAW_ROWS * D;  // elements of one raw block ([67][128] bf16 of q, k or v)
+static_assert((RAW_PART * 2) % 128 == 0, "raw blocks stay 128-byte aligned");
+
+// Tiled TMA load of a (channel, head, token) box of a [T][H][128] bf16 token tensor into shared memory,
+// completion counted on `bar`.  The channel coordinate is always 0; token coordinates outside [0, T) read
+// zeros.
+__device__ __forceinline__ void tma_load_tokens(void *dst, const CUtensorMap *map, int head, int token,
+                                                uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(head), "r"(token), "r"(smem_addr(bar))
+        : "memory");
+}
 
 __device__ __forceinline__ float log_sigmoid_fast(float x) {
     // log(sigmoid(x)) = min(x, 0) - log(1 + exp(-|x|)); absolute error ~1e-7, which is what the
@@ -536,7 +554,10 @@ __device__ __forceinline__ float log_sigmoid_fast(float x) {
     return fminf(x, 0.f) - __logf(1.f + __expf(-fabsf(x)));
 }
 
-__global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillArgs a, const Layout2 L) {
+__global__ void __launch_bounds__(NTI, 1)
+    prefill_intra_tc_kernel(const PrefillArgs a, const Layout2 L, const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, CC = 3 * D;
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
     float *kh = reinterpret_cast<float *>(sm + I_K);
     float *G = reinterpret_cast<float *>(sm + I_G);
     uint8_t *Vt = sm + I_VT;
-    uint16_t *raw = reinterpret_cast<uint16_t *>(sm + I_RAW);  // [67][384] bf16, row = position p0 - 3 + row
+    uint16_t *raw = reinterpret_cast<uint16_t *>(sm + I_RAW);  // q, k, v blocks [67][128] bf16, row = position p0-3+row
     float *beta = reinterpret_cast<float *>(sm + I_MISC);
     float *eGm = beta + 64;     // exp(G_mid) per channel
     float *gtot = eGm + D;      // [4][128] partial sums of the cumulative decay
@@ -568,82 +589,51 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
     }
 
     // ---- P0: the chunk's raw q|k|v rows (and 3 rows of history) and decay logits into smem ----
-    // One 256-byte bulk copy per (row, tensor), issued by one thread each; rows without a source are
-    // zero-filled with ordinary stores.  Row `row` holds position p0 - 3 + row; history rows before the
-    // sequence start come from the source slot's stored window.
-    uint16_t *astage = reinterpret_cast<uint16_t *>(sm + I_VT);  // decay logits bf16 [64][128] (V^T comes later)
+    // Four tiled TMA loads: 67 token rows of q, k and v starting 3 tokens before the chunk (zeros before the
+    // first token), and the chunk's 64 rows of decay logits.  History rows that precede the sequence start
+    // are then replaced by the source slot's stored window (or zeros).  Rows past the chunk's last token hold
+    // whatever follows; every use of them is masked.
+    uint16_t *astage = reinterpret_cast<uint16_t *>(sm + I_G);  // decay logits bf16 [64][128] (G comes later)
     uint64_t *bar_in = bar + 1;
-    const int nrows = (kConvW - 1) + ntok;                        // rows with data
-    const int hist_src = (int)min((int64_t)nrows, max((int64_t)0, start - p0 + (kConvW - 1)));  // rows before start
     if (tid == 0) {
         mbar_init(bar_in, 1);
         fence_mbar_init();
-        const uint32_t bytes = (uint32_t)((nrows - (srcv >= 0 ? 0 : hist_src)) * 3 * 256 + ntok * 256);
-        mbar_arrive_expect_tx(bar_in, bytes);
+        mbar_arrive_expect_tx(bar_in, 3 * RAW_PART * 2 + CH * D * 2);
+        tma_load_tokens(raw, &tm_q, h, e.t0 - (kConvW - 1), bar_in);
+        tma_load_tokens(raw + RAW_PART, &tm_k, h, e.t0 - (kConvW - 1), bar_in);
+        tma_load_tokens(raw + 2 * RAW_PART, &tm_v, h, e.t0 - (kConvW - 1), bar_in);
+        tma_load_tokens(astage, &tm_a, h, e.t0, bar_in);
     }
-    __syncthreads();
-    if (tid < RAW_ROWS * 3) {
-        const int row = tid / 3, part = tid - (tid / 3) * 3;
-        const int64_t p = p0 - (kConvW - 1) + row;
-        uint16_t *dst = raw + row * CC + part * D;
-        const uint16_t *src = nullptr;
-        if (row < nrows) {
-            if (p >= start) {
-                const size_t t = (size_t)(ts + (p - start)) * H + h;
-                src = (part == 0 ? a.q : (part == 1 ? a.k : a.v)) + t * D;
-            } else if (srcv >= 0) {
-                src = a.conv + (((size_t)srcv * H + h) * (kConvW - 1) + (p - start + (kConvW - 1))) * CC + part * D;
-            }
-        }
-        if (src) {
-            bulk_g2s(dst, src, 256, bar_in);
-        } else {
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) d4[u] = make_uint4(0u, 0u, 0u, 0u);
-        }
-    } else if (tid >= 256 && tid < 256 + CH) {
-        const int r = tid - 256;
-        uint16_t *dst = astage + r * D;
-        if (r < ntok) {
-            bulk_g2s(dst, a.a + ((size_t)(e.t0 + r) * H + h) * D, 256, bar_in);
-        } else {
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) d4[u] = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
+    __syncthreads();  // no thread waits on bar_in (or reads the tensor-memory address) before it is initialised
+    const int hist_src = (int)min((int64_t)(kConvW - 1), max((int64_t)0, start - p0 + (kConvW - 1)));  // rows before start
+    // global loads that do not depend on the copies, issued before the wait: beta logit, conv weights
+    const uint16_t blogit = (tid < CH && tid < ntok) ? a.b[(size_t)(e.t0 + tid) * H + h] : (uint16_t)0;
+    const float4 w = tid < CC ? __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + tid) * kConvW))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
     if (__syncthreads_or(!mbar_wait(bar_in, 0))) {
         if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
         __syncthreads();
         if (warp == 0) umma::dealloc(*tmem_s, 256);
         return;
     }
-    for (int idx = tid; idx < CH * 16; idx += NTI) {  // log decay, 8 channels per item
-        const int r = idx >> 4, part = idx & 15;
-        const uint4 v = reinterpret_cast<const uint4 *>(astage + r * D)[part];
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-        float g8[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            g8[2 * q] = r < ntok ? log_sigmoid_fast(bf2f((uint16_t)(w4[q] & 0xffff))) : 0.f;
-            g8[2 * q + 1] = r < ntok ? log_sigmoid_fast(bf2f((uint16_t)(w4[q] >> 16))) : 0.f;
-        }
-        float4 *gd = reinterpret_cast<float4 *>(G + r * D + part * 8);
-        gd[0] = make_float4(g8[0], g8[1], g8[2], g8[3]);
-        gd[1] = make_float4(g8[4], g8[5], g8[6], g8[7]);
+    for (int idx = tid; idx < hist_src * CC; idx += NTI) {  // history rows before the sequence start
+        const int row = idx / CC, ch = idx - (idx / CC) * CC;
+        const int64_t p = p0 - (kConvW - 1) + row;
+        raw[(ch >> 7) * RAW_PART + row * D + (ch & 127)] =
+            srcv >= 0 ? a.conv[(((size_t)srcv * H + h) * (kConvW - 1) + (p - start + (kConvW - 1))) * CC + ch]
+                      : (uint16_t)0;
     }
-    if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(a.b[(size_t)(e.t0 + tid) * H + h])) : 0.f;
+    if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(blogit)) : 0.f;
     __syncthreads();
     // ---- P1: causal conv + SiLU, one channel per thread along the chunk (window in registers) ----
     if (tid < CC) {
         const int ch = tid;
-        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
-        float h0 = bf2f(raw[ch]), h1 = bf2f(raw[CC + ch]), h2 = bf2f(raw[2 * CC + ch]);
+        const uint16_t *rc = raw + (ch >> 7) * RAW_PART + (ch & 127);  // this channel's column of its block
+        float h0 = bf2f(rc[0]), h1 = bf2f(rc[D]), h2 = bf2f(rc[2 * D]);
         for (int r0 = 0; r0 < CH; r0 += 8) {
             float xs8[8], ob[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) xs8[u] = bf2f(raw[(r0 + u + 3) * CC + ch]);  // all taps before any store
+            for (int u = 0; u < 8; ++u) xs8[u] = bf2f(rc[(r0 + u + 3) * D]);  // all taps before any store
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const float x = xs8[u];
@@ -669,29 +659,61 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
     __syncthreads();
     // raw rows of positions pend-3 .. pend-1 (the conv window after this chunk), kept past P2
     uint4 *wstash = reinterpret_cast<uint4 *>(sm + I_MISC + 3200);
-    if (tid < 3 * CC / 8) wstash[tid] = reinterpret_cast<const uint4 *>(raw + ntok * CC)[tid];
-    for (int r = warp; r < ntok; r += NTI / 32) {
-        const float nq = warp_dot_array(qh + r * D, qh + r * D, D);
-        const float nk = warp_dot_array(kh + r * D, kh + r * D, D);
-        const float rq = rsqrtf(nq + a.l2_eps), rk = rsqrtf(nk + a.l2_eps);
-        for (int i = lane; i < D; i += 32) {
-            qh[r * D + i] *= rq;
-            kh[r * D + i] *= rk;
+    if (tid < 3 * CC / 8) {  // [3][q|k|v] rows, the layout of a stored window
+        const int r3 = tid / (CC / 8), rem = tid - r3 * (CC / 8), part = rem >> 4, unit = rem & 15;
+        wstash[tid] = reinterpret_cast<const uint4 *>(raw + part * RAW_PART + (ntok + r3) * D)[unit];
+    }
+    {   // L2 norms: rows warp, warp + 16, warp + 32, warp + 48, their reductions interleaved
+        float sq[4], sk[4];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int r = warp + 16 * k4;
+            float aq = 0.f, ak = 0.f;
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+                const float xq = qh[r * D + lane + 32 * i], xk = kh[r * D + lane + 32 * i];
+                aq = fmaf(xq, xq, aq);
+                ak = fmaf(xk, xk, ak);
+            }
+            sq[k4] = aq;
+            sk[k4] = ak;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                sq[k4] += __shfl_xor_sync(0xffffffffu, sq[k4], o);
+                sk[k4] += __shfl_xor_sync(0xffffffffu, sk[k4], o);
+            }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int r = warp + 16 * k4;
+            if (r >= ntok) continue;
+            const float rq = rsqrtf(sq[k4] + a.l2_eps), rk = rsqrtf(sk[k4] + a.l2_eps);
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+                qh[r * D + lane + 32 * i] *= rq;
+                kh[r * D + lane + 32 * i] *= rk;
+            }
         }
     }
-    {   // cumulative log decay along the chunk: 4 threads per channel, 16 tokens each
+    {   // cumulative log decay along the chunk from the staged logits: 4 threads per channel, 16 tokens each,
+        // in registers; G overwrites the staging only after every logit has been read
         const int ch = tid & 127, qd = tid >> 7;
+        float g16[16];
         float acc = 0.f;
-        for (int r = 16 * qd; r < 16 * qd + 16; ++r) {
-            acc += G[r * D + ch];
-            G[r * D + ch] = acc;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int r = 16 * qd + u;
+            acc += r < ntok ? log_sigmoid_fast(bf2f(astage[r * D + ch])) : 0.f;
+            g16[u] = acc;
         }
         gtot[qd * D + ch] = acc;
         __syncthreads();
         float off = 0.f;
         for (int q2 = 0; q2 < qd; ++q2) off += gtot[q2 * D + ch];
-        if (qd > 0)
-            for (int r = 16 * qd; r < 16 * qd + 16; ++r) G[r * D + ch] += off;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) G[(16 * qd + u) * D + ch] = qd > 0 ? g16[u] + off : g16[u];
     }
     __syncthreads();
 
@@ -934,11 +956,11 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
     fence_proxy_async_smem();
     umma::fence_before();
     __syncthreads();
-    if (tid == 0) {  // -W and U' to the workspace; every bulk copy of this CTA completes before it exits
+    if (tid == 0) {  // -W and U' to the workspace; the CTA may exit once its shared memory has been read
         bulk_s2g(blk + WS_W, Wst, CH * D * 2);
         bulk_s2g(blk + WS_UP, Ust, CH * D * 4);
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read_all();
     }
     if (warp == 0) umma::dealloc(tmem, 256);
 
@@ -968,22 +990,46 @@ __global__ void __launch_bounds__(NTI, 1) prefill_intra_tc_kernel(const PrefillA
 namespace tc {
 
 // State kernel smem (bytes, from a 1024-aligned base)
-constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand of U^T += S^T (-W)^T, O^T = S^T Q+^T
+constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand of U^T = S^T (-W)^T, O^T = S^T Q+^T
 constexpr uint32_t S_OPS = 32768;     // one chunk's workspace block (Qk, -W, Q+, Ktil^T, gl, U'), WS_BLOCK bytes
 constexpr uint32_t S_UT32 = 140288;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil
 constexpr uint32_t S_UT16 = 173056;   // U^T bf16 tile [128 j][64 r]: A operand of O^T += U^T Qk^T
 constexpr uint32_t S_OST = 189440;    // O staging fp32 [64 r][OST] (row stride 132: 16-byte rows, conflict-free)
 constexpr int OST = 132;
 constexpr uint32_t S_NW = 223232;     // RMSNorm weight [128]
-constexpr uint32_t S_MISC = 223744;   // barriers, tensor-memory address
+constexpr uint32_t S_GLN = 223744;    // exp(G_last) of the next chunk [128]
+constexpr uint32_t S_MISC = 224256;   // barriers, tensor-memory address
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
 static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0 && S_UT16 % 1024 == 0, "state smem layout");
 static_assert(S_OST + CH * OST * 4 <= S_NW, "state smem layout");
+constexpr int NTS = 384;              // warps 0-7: the state chain; warps 8-11: the output epilogue
 
 // TMEM columns: S^T [0,128), U^T [128,192), O^T [192,256)
 constexpr uint32_t T_S = 0, T_U = 128, T_O = 192;
 
-__global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillArgs a, const Layout2 L) {
+// Barrier 1 over the 256 threads of the state warps (the output warps run their own loop).
+__device__ __forceinline__ void state_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool state_sync_or(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 1, 256, pi;\n selp.u32 %0, 1, 0, po;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)p)
+        : "memory");
+    return r != 0;
+}
+
+// The sequential chunk pass of one (sequence, head).  The state warps run the recurrence with S^T in tensor
+// memory, kept decayed by the NEXT chunk's exp(G_last) so that the chunk update is one accumulating MMA:
+//   U^T  = S^T (-W)^T                 (MMA, no accumulate)      O^T  = S^T Q+^T
+//   U    = U' + U^T read back         -> tf32 / bf16 operand tiles
+//   O^T += U^T Qk^T                   S^T += U^T Ktil           (MMAs; S^T already holds S^T diag(exp(G_last)))
+//   S pass: bf16 operand tile of the new S, checkpoint, then S^T diag(exp(G_last of the next chunk)) back to
+//   tensor memory (or the final state to dst).
+// The O tile goes through a staging buffer to the output warps, which apply the gated RMSNorm and store y
+// while the state warps go on with the next chunk.  The chunk block arrives in three bulk copies, each issued
+// as soon as the previous chunk no longer reads its region.
+__global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillArgs a, const Layout2 L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, CC = 3 * D;
@@ -991,17 +1037,20 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
     const int32_t flag = wsp<int32_t>(a, L.off_flags)[n];
     if (flag & kSeqInvalid) return;
     const int src = a.src[n], dst = a.dst[n];  // validated by the table kernel
-    const int quad = warp & 3, half = warp >> 2;
-    const int j = 32 * quad + lane;            // this thread's value channel = tensor-memory lane
-    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
     uint8_t *Sst = sm + S_ST;
     uint8_t *ops = sm + S_OPS;
     uint8_t *Ut32 = sm + S_UT32;
     uint8_t *Ut16 = sm + S_UT16;
     float *Ost = reinterpret_cast<float *>(sm + S_OST);
     float *nw = reinterpret_cast<float *>(sm + S_NW);
-    uint64_t *bar_ops = reinterpret_cast<uint64_t *>(sm + S_MISC);
-    uint64_t *bar_mma = bar_ops + 1;
+    float *gln = reinterpret_cast<float *>(sm + S_GLN);
+    uint64_t *bar_w = reinterpret_cast<uint64_t *>(sm + S_MISC);  // -W and Q+ of a chunk
+    uint64_t *bar_u = bar_w + 1;                                    // U'
+    uint64_t *bar_b = bar_w + 2;                                    // Qk and Ktil^T (+ exp(G_last))
+    uint64_t *bar_mma = bar_w + 3;
+    uint64_t *bar_full = bar_w + 4;   // O staged: one arrival per state warp
+    uint64_t *bar_empty = bar_w + 5;  // O consumed: one arrival per output warp
+    uint64_t *bar_o = bar_w + 6;      // the O^T MMAs of a chunk
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
     const int64_t start = a.start_pos[n];
     const int32_t c0 = wsp<int32_t>(a, L.off_seqc)[n], c1 = wsp<int32_t>(a, L.off_seqc)[n + 1];
@@ -1009,16 +1058,36 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
     const int64_t *pos = wsp<int64_t>(a, L.off_pos);
     const uint8_t *blk0 = reinterpret_cast<const uint8_t *>(a.ws) + L.off_blk;
     auto blk_of = [&](int32_t c) { return blk0 + ((size_t)c * H + h) * WS_BLOCK; };
+    // -W and Q+ complete one phase of bar_w together: -W is copied as soon as the U^T MMAs are done with
+    // it, Q+ once every MMA of the chunk is (the O^T MMAs that read it are issued after the U^T commit)
+    auto issue_w = [&](int32_t c) {
+        mbar_arrive_expect_tx(bar_w, 2 * CH * D * 2);
+        bulk_g2s(ops + WS_W, blk_of(c) + WS_W, CH * D * 2, bar_w);
+    };
+    auto issue_qp = [&](int32_t c) { bulk_g2s(ops + WS_QP, blk_of(c) + WS_QP, CH * D * 2, bar_w); };
+    auto issue_u = [&](int32_t c) {
+        mbar_arrive_expect_tx(bar_u, CH * D * 4);
+        bulk_g2s(ops + WS_UP, blk_of(c) + WS_UP, CH * D * 4, bar_u);
+    };
+    auto issue_b = [&](int32_t c) {
+        mbar_arrive_expect_tx(bar_b, CH * CH * 2 + D * CH * 4 + D * 4);
+        bulk_g2s(ops + WS_QK, blk_of(c) + WS_QK, CH * CH * 2, bar_b);
+        bulk_g2s(ops + WS_KT, blk_of(c) + WS_KT, D * CH * 4 + D * 4, bar_b);  // Ktil^T and exp(G_last)
+    };
 
     if (warp == 0) umma::alloc(tmem_s, 256);
-    for (int jj = tid; jj < D; jj += NT) nw[jj] = __ldg(a.norm_w + jj);
+    for (int jj = tid; jj < D; jj += NTS) nw[jj] = __ldg(a.norm_w + jj);
     if (tid == 0) {
-        mbar_init(bar_ops, 1);
-        mbar_init(bar_mma, 1);
+        for (int b = 0; b < 4; ++b) mbar_init(bar_w + b, 1);
+        mbar_init(bar_o, 1);
+        mbar_init(bar_full, 8);
+        mbar_init(bar_empty, 4);
         fence_mbar_init();
         if (c0 < c1) {
-            mbar_arrive_expect_tx(bar_ops, WS_BLOCK);
-            bulk_g2s(ops, blk_of(c0), WS_BLOCK, bar_ops);
+            issue_w(c0);
+            issue_qp(c0);
+            issue_u(c0);
+            issue_b(c0);
         }
     }
     umma::fence_before();
@@ -1026,170 +1095,222 @@ __global__ void __launch_bounds__(NT, 1) prefill_state_tc_kernel(const PrefillAr
     umma::fence_after();
     const uint32_t tmem = *tmem_s;
 
-    // initial state: S^T in tensor memory (lane j, column i) and its bf16 operand tile
-    {
-        float v[32];
-        for (int part = 0; part < 2; ++part) {
-            const int i0 = 64 * half + 32 * part;
-#pragma unroll
-            for (int t = 0; t < 32; ++t)
-                v[t] = src >= 0 ? load_state(a.S, a.state_bf16, (((size_t)src * H + h) * D + i0 + t) * D + j) : 0.f;
-            umma::st32(tmem + lane_off + T_S + i0, v);
-#pragma unroll
-            for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
-        }
-    }
-    uint32_t ph_ops = 0, ph_mma = 0;
-    bool ok = true;
-    for (int32_t c = c0; c < c1 && ok; ++c) {
-        const ChunkEnt e = ent[c];
-        const int64_t pend = pos[c] + e.n;
-        int ck = -1;  // checkpoint slot of this chunk's end (looked up early; used after the state update)
-        if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
-            const int64_t jj = pend / a.interval - start / a.interval - 1;
-            const int s_ = a.ckpt_slots[a.ckpt_offsets[n] + jj];
-            if (s_ >= 0 && s_ < a.num_slots) ck = s_;
-        }
-        // the output gate of this warp's tokens (warp + 8k), channels 4*lane .. 4*lane+3, fetched early
-        uint2 zr[8];
-#pragma unroll
-        for (int k8 = 0; k8 < 8; ++k8) {
-            const int r = warp + 8 * k8;
-            zr[k8] = (a.z && r < e.n)
-                         ? __ldg(reinterpret_cast<const uint2 *>(a.z + ((size_t)(e.t0 + r) * H + h) * D) + lane)
-                         : make_uint2(0u, 0u);
-        }
-        ok = mbar_wait(bar_ops, ph_ops);
-        ph_ops ^= 1;
-        // U' -> U^T columns of tensor memory (lane j, column r)
-        if (ok) {
-            float v[32];
-            const float *up = reinterpret_cast<const float *>(ops + WS_UP);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = up[(32 * half + t) * D + j];
-            umma::st32(tmem + lane_off + T_U + 32 * half, v);
-        }
-        fence_proxy_async_smem();
-        umma::fence_before();
-        __syncthreads();
-        umma::fence_after();
-        if (tid == 0 && ok) {
-            const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint64_t as = umma::sdesc_k(Sst, D, ks);
-                umma::mma_bf16(tmem + T_U, as, umma::sdesc_k(ops + WS_W, CH, ks), idp, true);   // U^T += S^T (-W)^T
-                umma::mma_bf16(tmem + T_O, as, umma::sdesc_k(ops + WS_QP, CH, ks), idp, ks > 0); // O^T = S^T Q+^T
-            }
-            umma::commit(bar_mma);
-        }
-        ok = __syncthreads_or(!ok) == 0 && wait_all(bar_mma, ph_mma);
-        ph_mma ^= 1;
-        umma::fence_after();
-        if (!ok) break;
-        // U^T -> its tf32 and bf16 operand tiles; decay the state columns by exp(G_last)
+    if (warp < 8) {
+        // ================================ state warps ================================
+        const int quad = warp & 3, half = warp >> 2;
+        const int j = 32 * quad + lane;  // this thread's value channel = tensor-memory lane
+        const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+        // initial state: its bf16 operand tile, and S^T diag(exp(G_last of the first chunk)) in tensor memory
         {
-            float v[32];
-            umma::ld32(tmem + lane_off + T_U + 32 * half, v);
-#pragma unroll
-            for (int t = 0; t < 32; t += 4) umma::st_tf32x4(Ut32, D, j, 32 * half + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
-#pragma unroll
-            for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Ut16, D, j, 32 * half + t, v + t);
-            const float *gl = reinterpret_cast<const float *>(ops + WS_GL);
-            for (int part = 0; part < 2; ++part) {
-                const int i0 = 64 * half + 32 * part;
-                umma::ld32(tmem + lane_off + T_S + i0, v);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] *= gl[i0 + t];
-                umma::st32(tmem + lane_off + T_S + i0, v);
-            }
-        }
-        fence_proxy_async_smem();
-        umma::fence_before();
-        __syncthreads();
-        umma::fence_after();
-        if (tid == 0) {
-            const uint32_t ido = umma::idesc(umma::kBF16, 128, CH);
-            for (int ks = 0; ks < CH / 16; ++ks)  // O^T += U^T Qk^T
-                umma::mma_bf16(tmem + T_O, umma::sdesc_k(Ut16, D, ks), umma::sdesc_k(ops + WS_QK, CH, ks), ido, true);
-            const uint32_t ids = umma::idesc(umma::kTF32, 128, D);
-            for (int ks = 0; ks < CH / 8; ++ks)   // S^T += U^T Ktil
-                umma::mma_tf32(tmem + T_S, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_KT, D, ks), ids, true);
-            umma::commit(bar_mma);
-        }
-        ok = wait_all(bar_mma, ph_mma);
-        ph_mma ^= 1;
-        umma::fence_after();
-        if (!ok) break;
-        // the operand buffer is free: start the next chunk's copy
-        if (tid == 0 && c + 1 < c1) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar_ops, WS_BLOCK);
-            bulk_g2s(ops, blk_of(c + 1), WS_BLOCK, bar_ops);
-        }
-        // outputs: O^T -> staging -> gated RMSNorm -> y
-        {
-            float v[32];
-            umma::ld32(tmem + lane_off + T_O + 32 * half, v);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) Ost[(32 * half + t) * OST + j] = v[t];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k8 = 0; k8 < 8; ++k8) {  // one warp per token, 4 contiguous channels per lane
-            const int r = warp + 8 * k8;
-            const float4 o4 = *reinterpret_cast<const float4 *>(Ost + r * OST + 4 * lane);
-            float ss = o4.x * o4.x;
-            ss = fmaf(o4.y, o4.y, ss);
-            ss = fmaf(o4.z, o4.z, ss);
-            ss = fmaf(o4.w, o4.w, ss);
-            ss = warp_sum(ss);
-            const float rr = rsqrtf(ss * (1.0f / D) + a.rms_eps);
-            if (r < e.n) {
-                const float4 w4 = *reinterpret_cast<const float4 *>(nw + 4 * lane);
-                float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
-                if (a.z) {
-                    y0 *= sigmoid_gate(bf2f((uint16_t)(zr[k8].x & 0xffff)));
-                    y1 *= sigmoid_gate(bf2f((uint16_t)(zr[k8].x >> 16)));
-                    y2 *= sigmoid_gate(bf2f((uint16_t)(zr[k8].y & 0xffff)));
-                    y3 *= sigmoid_gate(bf2f((uint16_t)(zr[k8].y >> 16)));
-                }
-                *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
-                    make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
-                               (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
-            }
-        }
-        // new state: bf16 operand tile for the next chunk; checkpoint when this chunk ends on a boundary
-        {
+            const float *gl0 = c0 < c1 ? reinterpret_cast<const float *>(blk_of(c0) + WS_GL) : nullptr;
             float v[32];
             for (int part = 0; part < 2; ++part) {
                 const int i0 = 64 * half + 32 * part;
-                umma::ld32(tmem + lane_off + T_S + i0, v);
 #pragma unroll
-                for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
-                if (ck >= 0) {
+                for (int t = 0; t < 32; ++t)
+                    v[t] = src >= 0 ? load_state(a.S, a.state_bf16, (((size_t)src * H + h) * D + i0 + t) * D + j) : 0.f;
+                if (c0 == c1) {  // empty sequence: the state and window pass through unchanged
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
-                        store_state(a.S, a.state_bf16, (((size_t)ck * H + h) * D + i0 + t) * D + j, v[t]);
+                        store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
+                    continue;
                 }
+#pragma unroll
+                for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] *= __ldg(gl0 + i0 + t);
+                umma::st32(tmem + lane_off + T_S + i0, v);
+            }
+            if (c0 == c1) {
+                uint16_t *cw = a.conv + ((size_t)dst * H + h) * (kConvW - 1) * CC;
+                for (int idx = tid; idx < (kConvW - 1) * CC; idx += 256)
+                    cw[idx] = src >= 0 ? a.conv[((size_t)src * H + h) * (kConvW - 1) * CC + idx] : (uint16_t)0;
             }
         }
-        __syncthreads();  // staging and tiles are reused by the next chunk
-    }
-    if (!ok) {
-        if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
-    } else {
-        float v[32];
-        for (int part = 0; part < 2; ++part) {
-            const int i0 = 64 * half + 32 * part;
-            umma::ld32(tmem + lane_off + T_S + i0, v);
+        fence_proxy_async_smem();
+        umma::fence_before();
+        state_sync();
+        umma::fence_after();
+        uint32_t ph_w = 0, ph_u = 0, ph_b = 0, ph_m = 0, ph_o = 0;
+        bool ok = true;
+        for (int32_t c = c0; c < c1; ++c) {
+            const ChunkEnt e = ent[c];
+            const int64_t pend = pos[c] + e.n;
+            const bool has_next = c + 1 < c1;
+            int ck = -1;  // checkpoint slot of this chunk's end
+            if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
+                const int64_t jj = pend / a.interval - start / a.interval - 1;
+                const int s_ = a.ckpt_slots[a.ckpt_offsets[n] + jj];
+                if (s_ >= 0 && s_ < a.num_slots) ck = s_;
+            }
+            const float gnext = (tid < D && has_next) ? __ldg(reinterpret_cast<const float *>(blk_of(c + 1) + WS_GL) + tid)
+                                                      : 1.f;
+            // ---- U^T = S^T (-W)^T and O^T = S^T Q+^T (if -W / Q+ never arrive, nothing is committed and
+            //      every thread's bounded wait on bar_mma gives up) ----
+            if (tid == 0 && mbar_wait(bar_w, ph_w)) {
+                const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma::mma_bf16(tmem + T_U, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_W, CH, ks), idp, ks > 0);
+                umma::commit(bar_mma);  // U^T is read back first; the O^T MMAs complete meanwhile
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma::mma_bf16(tmem + T_O, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_QP, CH, ks), idp, ks > 0);
+            }
+            ph_w ^= 1;
+            ok = mbar_wait(bar_mma, ph_m);
+            ph_m ^= 1;
+            ok = !state_sync_or(!ok);
+            umma::fence_after();
+            if (!ok) break;
+            if (tid == 0 && has_next) issue_w(c + 1);  // the U^T MMAs no longer read -W
+            // ---- U = U' + U^T -> its tf32 and bf16 operand tiles ----
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_u, ph_u));  // warp-uniform: ld32 is a warp operation
+            ph_u ^= 1;
+            if (ok) {
+                float v[32];
+                umma::ld32(tmem + lane_off + T_U + 32 * half, v);
+                const float *up = reinterpret_cast<const float *>(ops + WS_UP);
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
-                store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
+                for (int t = 0; t < 32; ++t) v[t] += up[(32 * half + t) * D + j];
+#pragma unroll
+                for (int t = 0; t < 32; t += 4)
+                    umma::st_tf32x4(Ut32, D, j, 32 * half + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
+#pragma unroll
+                for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Ut16, D, j, 32 * half + t, v + t);
+            }
+            if (tid < D) gln[tid] = gnext;
+            fence_proxy_async_smem();
+            umma::fence_before();
+            ok = !state_sync_or(!ok);
+            umma::fence_after();
+            if (!ok) break;
+            // ---- O^T += U^T Qk^T and S^T += U^T Ktil ----
+            if (tid == 0) {
+                if (has_next) issue_u(c + 1);  // U' has been read by every thread
+                const bool okb = mbar_wait(bar_b, ph_b);
+                if (okb) {
+                    const uint32_t ids = umma::idesc(umma::kTF32, 128, D);
+                    for (int ks = 0; ks < CH / 8; ++ks)
+                        umma::mma_tf32(tmem + T_S, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_KT, D, ks), ids,
+                                       true);
+                    umma::commit(bar_mma);  // the S pass needs only S^T
+                    const uint32_t ido = umma::idesc(umma::kBF16, 128, CH);
+                    for (int ks = 0; ks < CH / 16; ++ks)
+                        umma::mma_bf16(tmem + T_O, umma::sdesc_k(Ut16, D, ks), umma::sdesc_k(ops + WS_QK, CH, ks), ido,
+                                       true);
+                    umma::commit(bar_o);    // covers both rounds of O^T MMAs
+                }
+            }
+            ph_b ^= 1;
+            ok = mbar_wait(bar_mma, ph_m);
+            ph_m ^= 1;
+            ok = !state_sync_or(!ok);
+            umma::fence_after();
+            if (!ok) break;
+            if (tid == 0 && has_next) issue_qp(c + 1);  // every MMA before the S^T commit is done: Q+ is free
+            // ---- S pass: bf16 tile of the new state, checkpoint, then decay by the next chunk (or the final store)
+            {
+                float v[32];
+                for (int part = 0; part < 2; ++part) {
+                    const int i0 = 64 * half + 32 * part;
+                    umma::ld32(tmem + lane_off + T_S + i0, v);
+                    if (ck >= 0) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            store_state(a.S, a.state_bf16, (((size_t)ck * H + h) * D + i0 + t) * D + j, v[t]);
+                    }
+                    if (has_next) {
+#pragma unroll
+                        for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] *= gln[i0 + t];
+                        umma::st32(tmem + lane_off + T_S + i0, v);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
+                    }
+                }
+            }
+            // ---- O^T -> the staging buffer of the output warps (once they have consumed the previous one) ----
+            if (c > c0) ok = __all_sync(0xffffffffu, mbar_wait(bar_empty, (uint32_t)(c - c0 - 1) & 1u));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_o, ph_o) && ok);
+            ph_o ^= 1;
+            umma::fence_after();
+            if (tid == 0 && ok && has_next) issue_b(c + 1);  // every MMA of this chunk is done: Qk, Ktil^T free
+            {
+                float v[32];
+                umma::ld32(tmem + lane_off + T_O + 32 * half, v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) Ost[(32 * half + t) * OST + j] = v[t];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(bar_full, 0);
+            fence_proxy_async_smem();
+            umma::fence_before();
+            ok = !state_sync_or(!ok);
+            umma::fence_after();
+            if (!ok) break;
         }
-        if (c0 == c1) {  // empty sequence: the window passes through unchanged
-            uint16_t *cw = a.conv + ((size_t)dst * H + h) * (kConvW - 1) * CC;
-            for (int idx = tid; idx < (kConvW - 1) * CC; idx += NT)
-                cw[idx] = src >= 0 ? a.conv[((size_t)src * H + h) * (kConvW - 1) * CC + idx] : (uint16_t)0;
+        if (!ok && tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+    } else {
+        // ================================ output warps ================================
+        const int ow = warp - 8;  // tokens ow, ow + 4, ..., one warp per token, 4 contiguous channels per lane
+        uint2 zr[16];
+        auto fetch_gates = [&](int32_t c) {  // the output gate of this warp's tokens of chunk c
+            const ChunkEnt e = ent[c];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int r = ow + 4 * k;
+                zr[k] = (a.z && r < e.n)
+                            ? __ldg(reinterpret_cast<const uint2 *>(a.z + ((size_t)(e.t0 + r) * H + h) * D) + lane)
+                            : make_uint2(0u, 0u);
+            }
+        };
+        if (c0 < c1) fetch_gates(c0);
+        for (int32_t c = c0; c < c1; ++c) {
+            const ChunkEnt e = ent[c];
+            if (!mbar_wait(bar_full, (uint32_t)(c - c0) & 1u)) {
+                if (lane == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+                break;
+            }
+            const float4 w4 = *reinterpret_cast<const float4 *>(nw + 4 * lane);
+            // all 16 rows are read before any y store (the stores could otherwise be taken to alias the
+            // staging), and their reductions are interleaved
+            float4 o16[16];
+            float ss[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                o16[k] = *reinterpret_cast<const float4 *>(Ost + (ow + 4 * k) * OST + 4 * lane);
+                ss[k] = o16[k].x * o16[k].x;
+                ss[k] = fmaf(o16[k].y, o16[k].y, ss[k]);
+                ss[k] = fmaf(o16[k].z, o16[k].z, ss[k]);
+                ss[k] = fmaf(o16[k].w, o16[k].w, ss[k]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int k = 0; k < 16; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], o);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(bar_empty, 0);  // the staging has been read
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int r = ow + 4 * k;
+                const float4 o4 = o16[k];
+                const float rr = rsqrtf(ss[k] * (1.0f / D) + a.rms_eps);
+                if (r < e.n) {
+                    float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
+                    if (a.z) {
+                        y0 *= sigmoid_gate(bf2f((uint16_t)(zr[k].x & 0xffff)));
+                        y1 *= sigmoid_gate(bf2f((uint16_t)(zr[k].x >> 16)));
+                        y2 *= sigmoid_gate(bf2f((uint16_t)(zr[k].y & 0xffff)));
+                        y3 *= sigmoid_gate(bf2f((uint16_t)(zr[k].y >> 16)));
+                    }
+                    *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
+                        make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
+                                   (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
+                }
+            }
+            if (c + 1 < c1) fetch_gates(c + 1);
         }
     }
     umma::fence_before();
@@ -1213,6 +1334,37 @@ size_t prefill_workspace_bytes(int H, int dk, int dv, int nseq, int64_t total_to
     return make_layout(H, dk, dv, nseq, total_tokens, chunk).total;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against the driver library).
+static EncodeTiledFn tensor_map_encoder() {
+    static std::atomic<EncodeTiledFn> cached{nullptr};
+    EncodeTiledFn f = cached.load(std::memory_order_acquire);
+    if (f) return f;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+        return nullptr;
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    cached.store(f, std::memory_order_release);
+    return f;
+}
+
+// A [T][H][128] bf16 token tensor as a 3-D map (channel, head, token) with boxes of 128 channels x 1 head x
+// `rows` tokens; out-of-range tokens read as zeros.
+static bool token_map(EncodeTiledFn enc, CUtensorMap *m, const void *base, int H, int64_t T, int rows) {
+    const cuuint64_t dims[3] = {(cuuint64_t)tc::D, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)tc::D * 2, (cuuint64_t)H * tc::D * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)tc::D, 1u, (cuuint32_t)rows};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     const tc::Layout2 L2 = tc::make_layout2(a.H, a.nseq, a.total_tokens);
     static int attr_done[64] = {0};
@@ -1229,11 +1381,19 @@ static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     if (L2.maxc > 0x7fffffffLL || a.H > 65535) return fail(KDA_ERR_INVALID_ARG, "prefill: grid too large");
     prefill_table_kernel<<<1, kMaxSeqThreads, 0, st>>>(a, tc::as_layout(L2));
     if (a.total_tokens > 0) {
+        const EncodeTiledFn enc = tensor_map_encoder();
+        if (!enc) return fail(KDA_ERR_CUDA, "prefill: cuTensorMapEncodeTiled is not available");
+        CUtensorMap tq, tk, tv, ta;
+        if (!token_map(enc, &tq, a.q, a.H, a.total_tokens, tc::RAW_ROWS) ||
+            !token_map(enc, &tk, a.k, a.H, a.total_tokens, tc::RAW_ROWS) ||
+            !token_map(enc, &tv, a.v, a.H, a.total_tokens, tc::RAW_ROWS) ||
+            !token_map(enc, &ta, a.a, a.H, a.total_tokens, tc::CH))
+            return fail(KDA_ERR_CUDA, "prefill: tensor map encoding failed");
         dim3 gi((unsigned)L2.maxc, a.H);
-        tc::prefill_intra_tc_kernel<<<gi, tc::NTI, tc::I_SMEM, st>>>(a, L2);
+        tc::prefill_intra_tc_kernel<<<gi, tc::NTI, tc::I_SMEM, st>>>(a, L2, tq, tk, tv, ta);
     }
     dim3 gs(a.nseq, a.H);
-    tc::prefill_state_tc_kernel<<<gs, tc::NT, tc::S_SMEM, st>>>(a, L2);
+    tc::prefill_state_tc_kernel<<<gs, tc::NTS, tc::S_SMEM, st>>>(a, L2);
     return launch_result("prefill (tensor-core path) launch");
 }
 
