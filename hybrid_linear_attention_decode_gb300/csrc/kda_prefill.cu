@@ -526,7 +526,7 @@ constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_T = 163840;
 constexpr uint32_t I_INV = 0;          // Inv fp32 [64][64] over q^ (free after the Qk copy-out)
 constexpr uint32_t I_QKS_SLOW = 148480; // Qk staging of the wide-decay path (q^ is still read there)
 constexpr uint32_t I_MISC = 184320;   // beta, exp(G_mid), decay partial sums, barrier, tmem address, window stash
-constexpr uint32_t I_SMEM = I_MISC + 6144 + 1024;  // + alignment slack
+constexpr uint32_t I_SMEM = I_MISC + 7168 + 1024;  // + alignment slack
 constexpr int RAW_ROWS = CH + kConvW - 1;           // 3 history rows + 64 tokens
 constexpr int AST = 68;                             // row stride of A in smem (padded against bank conflicts)
 static_assert(I_A + CH * AST * 4 <= I_QKS_SLOW && I_QKS_SLOW + CH * CH * 2 <= I_T, "A and slow Qk staging");
@@ -535,6 +535,12 @@ static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
 constexpr int NTI = 512;  // intra kernel threads
 constexpr int RAW_PART = RAW_ROWS * D;  // elements of one raw block ([67][128] bf16 of q, k or v)
 static_assert((RAW_PART * 2) % 128 == 0, "raw blocks stay 128-byte aligned");
+
+// What the intra kernel needs to know about one work item beyond (chunk, head).
+struct ItemMeta {
+    int32_t seq, t0, n, srcv;    // sequence, first token, tokens, source slot
+    int64_t p0, start, ts, len;  // first position, the sequence's start position, first token and length
+};
 
 // Tiled TMA load of a (channel, head, token) box of a [T][H][128] bf16 token tensor into shared memory,
 // completion counted on `bar`.  The channel coordinate is always 0; token coordinates outside [0, T) read
@@ -561,71 +567,98 @@ __global__ void __launch_bounds__(NTI, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, CC = 3 * D;
-    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (c >= *wsp<int32_t>(a, L.off_cnt)) return;
-    const ChunkEnt e = wsp<ChunkEnt>(a, L.off_ent)[c];
-    const int64_t p0 = wsp<int64_t>(a, L.off_pos)[c];
-    const int n = e.seq, ntok = e.n;
-    const int64_t start = a.start_pos[n], ts = a.cu_seqlens[n];
-    const int64_t len = (int64_t)a.cu_seqlens[n + 1] - ts;
-    const int srcv = a.src[n];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int total = *wsp<int32_t>(a, L.off_cnt) * H;  // work items (chunk, head), head fastest
+    if ((int)blockIdx.x >= total) return;
 
     float *qh = reinterpret_cast<float *>(sm + I_Q);
     float *kh = reinterpret_cast<float *>(sm + I_K);
     float *G = reinterpret_cast<float *>(sm + I_G);
     uint8_t *Vt = sm + I_VT;
     uint16_t *raw = reinterpret_cast<uint16_t *>(sm + I_RAW);  // q, k, v blocks [67][128] bf16, row = position p0-3+row
+    uint16_t *astage = reinterpret_cast<uint16_t *>(sm + I_G);  // decay logits bf16 [64][128] (G comes later)
     float *beta = reinterpret_cast<float *>(sm + I_MISC);
     float *eGm = beta + 64;     // exp(G_mid) per channel
     float *gtot = eGm + D;      // [4][128] partial sums of the cumulative decay
+    ItemMeta *meta = reinterpret_cast<ItemMeta *>(sm + I_MISC + 2816);  // [2], by item parity
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + I_MISC + 3072);
+    uint64_t *bar_in = bar + 1;
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + I_MISC + 3136);
-    uint8_t *blk = reinterpret_cast<uint8_t *>(a.ws) + L.off_blk + ((size_t)c * H + h) * WS_BLOCK;
+    uint4 *wstash = reinterpret_cast<uint4 *>(sm + I_MISC + 3200);  // raw rows of the window after the chunk
+
+    // Item metadata from global memory (one thread; dependent loads).
+    auto load_meta = [&](int item, ItemMeta *m) {
+        const int c = item / H;
+        const ChunkEnt e = wsp<ChunkEnt>(a, L.off_ent)[c];
+        m->seq = e.seq;
+        m->t0 = e.t0;
+        m->n = e.n;
+        m->p0 = wsp<int64_t>(a, L.off_pos)[c];
+        m->start = a.start_pos[e.seq];
+        m->ts = a.cu_seqlens[e.seq];
+        m->len = (int64_t)a.cu_seqlens[e.seq + 1] - m->ts;
+        m->srcv = a.src[e.seq];
+    };
+    // TMA loads of an item's rows: 67 token rows of q, k and v starting 3 tokens before the chunk (zeros
+    // before the first token), and separately (its region frees later) the chunk's 64 rows of decay logits.
+    // Both count on one phase of bar_in; rows past the chunk's last token hold whatever follows and every
+    // use of them is masked.
+    auto issue_rows = [&](const ItemMeta &m, int h) {
+        mbar_arrive_expect_tx(bar_in, 3 * RAW_PART * 2 + CH * D * 2);
+        tma_load_tokens(raw, &tm_q, h, m.t0 - (kConvW - 1), bar_in);
+        tma_load_tokens(raw + RAW_PART, &tm_k, h, m.t0 - (kConvW - 1), bar_in);
+        tma_load_tokens(raw + 2 * RAW_PART, &tm_v, h, m.t0 - (kConvW - 1), bar_in);
+    };
+    auto issue_logits = [&](const ItemMeta &m, int h) { tma_load_tokens(astage, &tm_a, h, m.t0, bar_in); };
 
     if (warp == 0) umma::alloc(tmem_s, 256);
     if (tid == 0) {
         mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-
-    // ---- P0: the chunk's raw q|k|v rows (and 3 rows of history) and decay logits into smem ----
-    // Four tiled TMA loads: 67 token rows of q, k and v starting 3 tokens before the chunk (zeros before the
-    // first token), and the chunk's 64 rows of decay logits.  History rows that precede the sequence start
-    // are then replaced by the source slot's stored window (or zeros).  Rows past the chunk's last token hold
-    // whatever follows; every use of them is masked.
-    uint16_t *astage = reinterpret_cast<uint16_t *>(sm + I_G);  // decay logits bf16 [64][128] (G comes later)
-    uint64_t *bar_in = bar + 1;
-    if (tid == 0) {
         mbar_init(bar_in, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_in, 3 * RAW_PART * 2 + CH * D * 2);
-        tma_load_tokens(raw, &tm_q, h, e.t0 - (kConvW - 1), bar_in);
-        tma_load_tokens(raw + RAW_PART, &tm_k, h, e.t0 - (kConvW - 1), bar_in);
-        tma_load_tokens(raw + 2 * RAW_PART, &tm_v, h, e.t0 - (kConvW - 1), bar_in);
-        tma_load_tokens(astage, &tm_a, h, e.t0, bar_in);
+        load_meta(blockIdx.x, &meta[0]);
+        issue_rows(meta[0], (int)blockIdx.x % H);
+        issue_logits(meta[0], (int)blockIdx.x % H);
     }
-    __syncthreads();  // no thread waits on bar_in (or reads the tensor-memory address) before it is initialised
-    const int hist_src = (int)min((int64_t)(kConvW - 1), max((int64_t)0, start - p0 + (kConvW - 1)));  // rows before start
-    // global loads that do not depend on the copies, issued before the wait: beta logit, conv weights
-    const uint16_t blogit = (tid < CH && tid < ntok) ? a.b[(size_t)(e.t0 + tid) * H + h] : (uint16_t)0;
-    const float4 w = tid < CC ? __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + tid) * kConvW))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (__syncthreads_or(!mbar_wait(bar_in, 0))) {
-        if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
-        __syncthreads();
-        if (warp == 0) umma::dealloc(*tmem_s, 256);
-        return;
+    __syncthreads();  // barriers, the tensor-memory address and the first item's metadata are in place
+    const uint32_t tmem = *tmem_s;
+    uint32_t phase = 0, ph_in = 0;
+    bool ok = true, in_flight = true;  // in_flight: row loads issued and not yet waited for (thread 0's view)
+    // the first item's beta logit and conv weights; later items get theirs prefetched by the item before
+    uint16_t blogit = 0;
+    float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+    {
+        const int h0 = (int)blockIdx.x % H;
+        if (tid < CH && tid < meta[0].n) blogit = a.b[(size_t)(meta[0].t0 + tid) * H + h0];
+        if (tid < CC) w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h0 * CC + tid) * kConvW));
     }
-    for (int idx = tid; idx < hist_src * CC; idx += NTI) {  // history rows before the sequence start
-        const int row = idx / CC, ch = idx - (idx / CC) * CC;
-        const int64_t p = p0 - (kConvW - 1) + row;
-        raw[(ch >> 7) * RAW_PART + row * D + (ch & 127)] =
-            srcv >= 0 ? a.conv[(((size_t)srcv * H + h) * (kConvW - 1) + (p - start + (kConvW - 1))) * CC + ch]
-                      : (uint16_t)0;
+
+    for (int item = blockIdx.x, it = 0; item < total; item += gridDim.x, ++it) {
+    const int c = item / H, h = item - (item / H) * H;
+    const int next = item + gridDim.x;
+    const bool has_next = next < total;
+    const int ntok = meta[it & 1].n;
+    uint8_t *blk = reinterpret_cast<uint8_t *>(a.ws) + L.off_blk + ((size_t)c * H + h) * WS_BLOCK;
+    ok = !__syncthreads_or(!mbar_wait(bar_in, ph_in));
+    if (!ok) break;  // the loads stay in flight: the exit path waits for them once more
+    ph_in ^= 1;
+    if (tid == 0) in_flight = false;
+    {   // history rows before the sequence start: the source slot's stored window, or zeros
+        const ItemMeta mt = meta[it & 1];
+        const int hist_src = (int)min((int64_t)(kConvW - 1), max((int64_t)0, mt.start - mt.p0 + (kConvW - 1)));
+        for (int idx = tid; idx < hist_src * CC; idx += NTI) {
+            const int row = idx / CC, ch = idx - (idx / CC) * CC;
+            const int64_t p = mt.p0 - (kConvW - 1) + row;
+            raw[(ch >> 7) * RAW_PART + row * D + (ch & 127)] =
+                mt.srcv >= 0
+                    ? a.conv[(((size_t)mt.srcv * H + h) * (kConvW - 1) + (p - mt.start + (kConvW - 1))) * CC + ch]
+                    : (uint16_t)0;
+        }
     }
     if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(blogit)) : 0.f;
     __syncthreads();
     // ---- P1: causal conv + SiLU, one channel per thread along the chunk (window in registers) ----
+    if (tid == NTI - 1 && has_next) load_meta(next, &meta[(it + 1) & 1]);  // warp 15 has no channel to convolve
     if (tid < CC) {
         const int ch = tid;
         const uint16_t *rc = raw + (ch >> 7) * RAW_PART + (ch & 127);  // this channel's column of its block
@@ -658,7 +691,6 @@ __global__ void __launch_bounds__(NTI, 1)
     }
     __syncthreads();
     // raw rows of positions pend-3 .. pend-1 (the conv window after this chunk), kept past P2
-    uint4 *wstash = reinterpret_cast<uint4 *>(sm + I_MISC + 3200);
     if (tid < 3 * CC / 8) {  // [3][q|k|v] rows, the layout of a stored window
         const int r3 = tid / (CC / 8), rem = tid - r3 * (CC / 8), part = rem >> 4, unit = rem & 15;
         wstash[tid] = reinterpret_cast<const uint4 *>(raw + part * RAW_PART + (ntok + r3) * D)[unit];
@@ -768,9 +800,6 @@ __global__ void __launch_bounds__(NTI, 1)
     umma::fence_before();
     __syncthreads();
     umma::fence_after();
-    const uint32_t tmem = *tmem_s;
-    uint32_t phase = 0;
-    bool ok = true;
     if (!slow) {
         if (tid == 0) {
             const uint32_t id = umma::idesc(umma::kBF16, 128, CH);
@@ -830,9 +859,8 @@ __global__ void __launch_bounds__(NTI, 1)
         }
     }
     if (__syncthreads_or(!ok)) {
-        if (tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
-        if (warp == 0) umma::dealloc(tmem, 256);
-        return;
+        ok = false;
+        break;
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -930,15 +958,7 @@ __global__ void __launch_bounds__(NTI, 1)
     ok = wait_all(bar, phase);
     phase ^= 1;
     umma::fence_after();
-    if (!ok) {
-        if (tid == 0) {
-            set_status(a.status, KDA_DEV_TIMEOUT);
-            bulk_wait_all();  // the Ktil^T copy still reads this CTA's shared memory
-        }
-        __syncthreads();
-        if (warp == 0) umma::dealloc(tmem, 256);
-        return;
-    }
+    if (!ok) break;
     // ---- P6: -W (bf16 tile [64 r][128 i]) and U' (fp32 [64 r][128 j]) via smem staging ----
     uint8_t *Wst = sm + I_K;
     float *Ust = reinterpret_cast<float *>(sm + I_G);
@@ -956,33 +976,63 @@ __global__ void __launch_bounds__(NTI, 1)
     fence_proxy_async_smem();
     umma::fence_before();
     __syncthreads();
-    if (tid == 0) {  // -W and U' to the workspace; the CTA may exit once its shared memory has been read
-        bulk_s2g(blk + WS_W, Wst, CH * D * 2);
+    // The next item's loads start here: its rows go to the raw region (every MMA is done and, once the
+    // Ktil^T copy has been read, nothing else lives there); its decay logits go to the G region once the U'
+    // copy below has read it.  Its beta logit and conv weights are fetched into registers meanwhile.
+    const ItemMeta mn = meta[(it + 1) & 1];
+    const int hn = next % H;
+    if (tid == 0) {
+        if (has_next) {
+            bulk_wait_read_all();  // the Ktil^T copy
+            issue_rows(mn, hn);
+        }
+        bulk_s2g(blk + WS_W, Wst, CH * D * 2);  // -W and U' to the workspace
         bulk_s2g(blk + WS_UP, Ust, CH * D * 4);
         bulk_commit();
         bulk_wait_read_all();
-    }
-    if (warp == 0) umma::dealloc(tmem, 256);
-
-    // raw conv windows at a checkpoint boundary / at the sequence end (as the SIMT path)
-    const int32_t flag = wsp<int32_t>(a, L.off_flags)[n];
-    const int64_t pend = p0 + ntok;
-    int wslot[2] = {-1, -1};
-    if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
-        const int64_t jj = pend / a.interval - start / a.interval - 1;
-        const int s_ = a.ckpt_slots[a.ckpt_offsets[n] + jj];
-        if (s_ >= a.num_slots || s_ < -1) {
-            if (tid == 0) set_status(a.status, KDA_DEV_BAD_SLOT);
-        } else {
-            wslot[0] = s_;
+        if (has_next) {
+            issue_logits(mn, hn);
+            in_flight = true;
         }
     }
-    if (pend == start + len) wslot[1] = a.dst[n];
-    for (int w = 0; w < 2; ++w) {
-        if (wslot[w] < 0) continue;
-        uint4 *cw = reinterpret_cast<uint4 *>(a.conv + ((size_t)wslot[w] * H + h) * (kConvW - 1) * CC);
-        if (tid < 3 * CC / 8) cw[tid] = wstash[tid];
+    if (has_next) {
+        blogit = (tid < CH && tid < mn.n) ? a.b[(size_t)(mn.t0 + tid) * H + hn] : (uint16_t)0;
+        if (tid < CC) w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)hn * CC + tid) * kConvW));
     }
+
+    // raw conv windows at a checkpoint boundary / at the sequence end (as the SIMT path); the item's
+    // metadata is read again here rather than kept in registers across the item
+    {
+        const ItemMeta me = meta[it & 1];
+        const int32_t flag = wsp<int32_t>(a, L.off_flags)[me.seq];
+        const int64_t pend = me.p0 + me.n;
+        int wslot[2] = {-1, -1};
+        if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
+            const int64_t jj = pend / a.interval - me.start / a.interval - 1;
+            const int s_ = a.ckpt_slots[a.ckpt_offsets[me.seq] + jj];
+            if (s_ >= a.num_slots || s_ < -1) {
+                if (tid == 0) set_status(a.status, KDA_DEV_BAD_SLOT);
+            } else {
+                wslot[0] = s_;
+            }
+        }
+        if (pend == me.start + me.len) wslot[1] = a.dst[me.seq];
+        const int hh = item - (item / H) * H;
+        for (int wi = 0; wi < 2; ++wi) {
+            if (wslot[wi] < 0) continue;
+            uint4 *cw = reinterpret_cast<uint4 *>(a.conv + ((size_t)wslot[wi] * H + hh) * (kConvW - 1) * CC);
+            if (tid < 3 * CC / 8) cw[tid] = wstash[tid];
+        }
+    }
+    __syncthreads();  // the window stash and this item's metadata are rewritten by the next item
+    }  // item loop
+    if (!ok && tid == 0) {
+        set_status(a.status, KDA_DEV_TIMEOUT);
+        bulk_wait_all();                          // copies that still read this CTA's shared memory
+        if (in_flight) mbar_wait(bar_in, ph_in);  // loads issued for an item that never ran (bounded)
+    }
+    __syncthreads();
+    if (warp == 0) umma::dealloc(tmem, 256);
 }
 
 }  // namespace tc
@@ -1133,15 +1183,30 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         umma::fence_after();
         uint32_t ph_w = 0, ph_u = 0, ph_b = 0, ph_m = 0, ph_o = 0;
         bool ok = true;
+        // checkpoint boundaries: a running next boundary, its slot fetched one boundary ahead (no division in
+        // the loop); chunk entries are fetched one chunk ahead
+        const bool want_ck = a.interval > 0 && !(flag & kSeqCkptBad) && c0 < c1;
+        const int64_t send = start + ((int64_t)a.cu_seqlens[n + 1] - a.cu_seqlens[n]);
+        int64_t next_b = want_ck ? (start / a.interval + 1) * a.interval : INT64_MAX;
+        const int32_t *cks = want_ck ? a.ckpt_slots + a.ckpt_offsets[n] : nullptr;
+        int jck = 0;
+        int ck_pre = (want_ck && next_b <= send) ? cks[0] : -1;
+        ChunkEnt e_nx = c0 < c1 ? ent[c0] : ChunkEnt{};
+        int64_t p_nx = c0 < c1 ? pos[c0] : 0;
         for (int32_t c = c0; c < c1; ++c) {
-            const ChunkEnt e = ent[c];
-            const int64_t pend = pos[c] + e.n;
+            const ChunkEnt e = e_nx;
+            const int64_t pend = p_nx + e.n;
             const bool has_next = c + 1 < c1;
+            if (has_next) {
+                e_nx = ent[c + 1];
+                p_nx = pos[c + 1];
+            }
             int ck = -1;  // checkpoint slot of this chunk's end
-            if (a.interval > 0 && pend % a.interval == 0 && !(flag & kSeqCkptBad)) {
-                const int64_t jj = pend / a.interval - start / a.interval - 1;
-                const int s_ = a.ckpt_slots[a.ckpt_offsets[n] + jj];
-                if (s_ >= 0 && s_ < a.num_slots) ck = s_;
+            if (pend == next_b) {
+                if (ck_pre >= 0 && ck_pre < a.num_slots) ck = ck_pre;
+                ++jck;
+                next_b += a.interval;
+                ck_pre = next_b <= send ? cks[jck] : -1;
             }
             const float gnext = (tid < D && has_next) ? __ldg(reinterpret_cast<const float *>(blk_of(c + 1) + WS_GL) + tid)
                                                       : 1.f;
@@ -1389,7 +1454,8 @@ static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
             !token_map(enc, &tv, a.v, a.H, a.total_tokens, tc::RAW_ROWS) ||
             !token_map(enc, &ta, a.a, a.H, a.total_tokens, tc::CH))
             return fail(KDA_ERR_CUDA, "prefill: tensor map encoding failed");
-        dim3 gi((unsigned)L2.maxc, a.H);
+        const long long items = (long long)L2.maxc * a.H;  // an upper bound; the kernel reads the real count
+        const unsigned gi = (unsigned)std::min<long long>(items, current_device_sms());  // one CTA per SM
         tc::prefill_intra_tc_kernel<<<gi, tc::NTI, tc::I_SMEM, st>>>(a, L2, tq, tk, tv, ta);
     }
     dim3 gs(a.nseq, a.H);
