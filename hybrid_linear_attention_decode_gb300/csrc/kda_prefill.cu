@@ -624,14 +624,9 @@ __global__ void __launch_bounds__(NTI, 1)
     const uint32_t tmem = *tmem_s;
     uint32_t phase = 0, ph_in = 0;
     bool ok = true, in_flight = true;  // in_flight: row loads issued and not yet waited for (thread 0's view)
-    // the first item's beta logit and conv weights; later items get theirs prefetched by the item before
-    uint16_t blogit = 0;
-    float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-    {
-        const int h0 = (int)blockIdx.x % H;
-        if (tid < CH && tid < meta[0].n) blogit = a.b[(size_t)(meta[0].t0 + tid) * H + h0];
-        if (tid < CC) w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h0 * CC + tid) * kConvW));
-    }
+    // the first item's beta logit; later items get theirs prefetched by the item before
+    uint16_t blogit = (tid < CH && tid < meta[0].n) ? a.b[(size_t)(meta[0].t0 + tid) * H + (int)blockIdx.x % H]
+                                                     : (uint16_t)0;
 
     for (int item = blockIdx.x, it = 0; item < total; item += gridDim.x, ++it) {
     const int c = item / H, h = item - (item / H) * H;
@@ -639,6 +634,9 @@ __global__ void __launch_bounds__(NTI, 1)
     const bool has_next = next < total;
     const int ntok = meta[it & 1].n;
     uint8_t *blk = reinterpret_cast<uint8_t *>(a.ws) + L.off_blk + ((size_t)c * H + h) * WS_BLOCK;
+    // conv weights of this head (fetched here rather than carried from the item before: registers)
+    const float4 w = tid < CC ? __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + tid) * kConvW))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
     ok = !__syncthreads_or(!mbar_wait(bar_in, ph_in));
     if (!ok) break;  // the loads stay in flight: the exit path waits for them once more
     ph_in ^= 1;
@@ -762,39 +760,53 @@ __global__ void __launch_bounds__(NTI, 1)
     uint8_t *X1 = sm + I_X1;
     uint8_t *Km = sm + I_KM;
     for (int idx = tid; idx < CH * 16; idx += NTI) {
-        const int r = idx >> 4, i0 = (idx & 15) * 8;  // 8 channels per item
-        float xk[8], xq[8], xm[8], xp[8], gv[8], kv[8], qv[8], gmv[8], egv[8];
-        *reinterpret_cast<float4 *>(gv) = *reinterpret_cast<const float4 *>(G + r * D + i0);
-        *reinterpret_cast<float4 *>(gv + 4) = *reinterpret_cast<const float4 *>(G + r * D + i0 + 4);
-        *reinterpret_cast<float4 *>(kv) = *reinterpret_cast<const float4 *>(kh + r * D + i0);
-        *reinterpret_cast<float4 *>(kv + 4) = *reinterpret_cast<const float4 *>(kh + r * D + i0 + 4);
-        *reinterpret_cast<float4 *>(qv) = *reinterpret_cast<const float4 *>(qh + r * D + i0);
-        *reinterpret_cast<float4 *>(qv + 4) = *reinterpret_cast<const float4 *>(qh + r * D + i0 + 4);
-        *reinterpret_cast<float4 *>(gmv) = *reinterpret_cast<const float4 *>(G + MID * D + i0);
-        *reinterpret_cast<float4 *>(gmv + 4) = *reinterpret_cast<const float4 *>(G + MID * D + i0 + 4);
-        *reinterpret_cast<float4 *>(egv) = *reinterpret_cast<const float4 *>(eGm + i0);
-        *reinterpret_cast<float4 *>(egv + 4) = *reinterpret_cast<const float4 *>(eGm + i0 + 4);
+        const int r = idx >> 4, i0 = (idx & 15) * 8;  // 8 channels per item, computed 4 at a time
+        uint32_t pk[4], pq[4], pm[4], pp[4];            // bf16 pairs of K+, Q+ (mid reference), K-, Q+ (chunk start)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const float g = gv[u], k_ = kv[u], q_ = qv[u];
-            float eq;
-            if (!slow) {
-                const float ep = __expf(g - gmv[u]);
-                xk[u] = k_ * ep;
-                xq[u] = q_ * ep;
-                xm[u] = k_ * __expf(gmv[u] - g);
-                eq = ep * egv[u];
-            } else {
-                eq = __expf(g);
+        for (int hq = 0; hq < 2; ++hq) {
+            const int ic = i0 + 4 * hq;
+            const float4 g4 = *reinterpret_cast<const float4 *>(G + r * D + ic);
+            const float4 k4 = *reinterpret_cast<const float4 *>(kh + r * D + ic);
+            const float4 q4 = *reinterpret_cast<const float4 *>(qh + r * D + ic);
+            const float4 m4 = *reinterpret_cast<const float4 *>(G + MID * D + ic);
+            const float4 e4 = *reinterpret_cast<const float4 *>(eGm + ic);
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+            const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, gmv[4] = {m4.x, m4.y, m4.z, m4.w};
+            const float egv[4] = {e4.x, e4.y, e4.z, e4.w};
+            float xk[4], xq[4], xm[4], xp[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float g = gv[u], k_ = kv[u], q_ = qv[u];
+                float eq;
+                if (!slow) {
+                    const float ep = __expf(g - gmv[u]);
+                    xk[u] = k_ * ep;
+                    xq[u] = q_ * ep;
+                    xm[u] = k_ * __expf(gmv[u] - g);
+                    eq = ep * egv[u];
+                } else {
+                    xk[u] = xq[u] = xm[u] = 0.f;
+                    eq = __expf(g);
+                }
+                xp[u] = a.scale * q_ * eq;
             }
-            xp[u] = a.scale * q_ * eq;
+            pk[2 * hq] = umma::pack_bf16(xk[0], xk[1]);
+            pk[2 * hq + 1] = umma::pack_bf16(xk[2], xk[3]);
+            pq[2 * hq] = umma::pack_bf16(xq[0], xq[1]);
+            pq[2 * hq + 1] = umma::pack_bf16(xq[2], xq[3]);
+            pm[2 * hq] = umma::pack_bf16(xm[0], xm[1]);
+            pm[2 * hq + 1] = umma::pack_bf16(xm[2], xm[3]);
+            pp[2 * hq] = umma::pack_bf16(xp[0], xp[1]);
+            pp[2 * hq + 1] = umma::pack_bf16(xp[2], xp[3]);
         }
         if (!slow) {
-            umma::st_bf16x8(X1, 128, r, i0, xk);
-            umma::st_bf16x8(X1, 128, CH + r, i0, xq);
-            umma::st_bf16x8(Km, CH, r, i0, xm);
+            *reinterpret_cast<uint4 *>(X1 + umma::sw128_offset<2>(128, r, i0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4 *>(X1 + umma::sw128_offset<2>(128, CH + r, i0)) =
+                make_uint4(pq[0], pq[1], pq[2], pq[3]);
+            *reinterpret_cast<uint4 *>(Km + umma::sw128_offset<2>(CH, r, i0)) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
         }
-        umma::st_bf16x8(blk + WS_QP, CH, r, i0, xp);
+        *reinterpret_cast<uint4 *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, i0)) =
+            make_uint4(pp[0], pp[1], pp[2], pp[3]);
     }
     fence_proxy_async_smem();
     umma::fence_before();
@@ -978,7 +990,7 @@ __global__ void __launch_bounds__(NTI, 1)
     __syncthreads();
     // The next item's loads start here: its rows go to the raw region (every MMA is done and, once the
     // Ktil^T copy has been read, nothing else lives there); its decay logits go to the G region once the U'
-    // copy below has read it.  Its beta logit and conv weights are fetched into registers meanwhile.
+    // copy below has read it.  Its beta logit is fetched into a register meanwhile.
     const ItemMeta mn = meta[(it + 1) & 1];
     const int hn = next % H;
     if (tid == 0) {
@@ -997,7 +1009,6 @@ __global__ void __launch_bounds__(NTI, 1)
     }
     if (has_next) {
         blogit = (tid < CH && tid < mn.n) ? a.b[(size_t)(mn.t0 + tid) * H + hn] : (uint16_t)0;
-        if (tid < CC) w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)hn * CC + tid) * kConvW));
     }
 
     // raw conv windows at a checkpoint boundary / at the sequence end (as the SIMT path); the item's
