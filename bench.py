@@ -358,6 +358,9 @@ def run_gpu(args):
     # ---- speculative verification: 5 tokens per request, every position kept
     decode_multi = run_decode_multi(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
 
+    # ---- the input projections feeding the prefill workload
+    projection = run_project(args, kda, torch, dev, stream, seed, ws)
+
     # ---- chunked prefill workload
     prefill = run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
 
@@ -379,6 +382,7 @@ def run_gpu(args):
             "gpu_launches": K,
             "decode_bf16_state": decode_bf16,
             "decode_multi_verify": decode_multi,
+            "projection": projection,
             "prefill": prefill}
     if rank == 0:
         if ws == 1 and not args.no_cpu_baseline:
@@ -387,6 +391,47 @@ def run_gpu(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+PROJ_HIDDEN = 4096  # hidden size of the synthetic layer whose projections feed the prefill workload
+
+
+def run_project(args, kda, torch, dev, stream, seed, ws):
+    """The six input projections of the prefill workload's 22528 tokens (hidden 4096 -> q, k, v, a, z, b for
+    H = 32, d = 128: 20512 features) as one GEMM, against the measured dense bf16 peak."""
+    T = int(sum(PRE_LENS))
+    N = kda.projection_width(H, DK, DV)
+    x_bits, w_bits = ki.projection_inputs(seed + 5, T, PROJ_HIDDEN, N)
+    x = bf16_dev(x_bits, dev)
+    w = bf16_dev(w_bits, dev)
+    e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)  # noqa: E731
+    q, k, v, a, z, b = e(T, H, DK), e(T, H, DK), e(T, H, DV), e(T, H, DK), e(T, H, DV), e(T, H)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run():
+        kda.kda_project_inputs(x, w, H, DK, DV, q, k, v, a, b, z, status, stream)
+
+    K, Wm = max(3, min(args.steps, 20)), max(3, args.warmup)
+    for _ in range(Wm):
+        run()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws) / K
+    if int(status.item()) != 0:
+        return {"error": f"device status {int(status.item())}"}
+    flops = 2.0 * T * PROJ_HIDDEN * N
+    tf = flops / (ms / 1000.0) / 1e12
+    _, bf16_peak, _, kind = measured_peaks()
+    return {"workload": f"input projections: {T} tokens x hidden {PROJ_HIDDEN} -> q, k, v, a, z, b for H=32, "
+                        f"d=128 ({N} features) in one GEMM, bf16 in, fp32 accumulate, bf16 out",
+            "tokens_per_s": T * ws / (ms / 1000.0), "ms_per_call": ms, "steps": K, "tflops": tf,
+            "bf16_peak_tflops": bf16_peak, "peak_kind": kind, "tensor_frac": tf / bf16_peak}
 
 
 MULTI_L = 5  # verify step: 4 draft tokens + 1
@@ -595,6 +640,9 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         print(f"profile case decode_multi: {n} launches")
+    elif args.profile == "project":
+        r = run_project(argparse.Namespace(steps=args.steps, warmup=args.warmup), kda, torch, dev, stream, seed, 1)
+        print(f"profile case project: {r}")
     else:
         pool = kda.StatePool.empty(512, H, DK, DV, W, device=dev)
         r = run_prefill(argparse.Namespace(steps=1, warmup=args.warmup), kda, torch, dev, stream, pool, prm, seed,
@@ -610,7 +658,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode_bf16", "decode_multi", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_bf16", "decode_multi", "project", "prefill"], default=None,
                     help="run a small case of one kernel for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:

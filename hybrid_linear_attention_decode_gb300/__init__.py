@@ -4,7 +4,8 @@ Argument marshalling only: every step of the path runs in the CUDA kernels behin
 ``include/kda.h``.  PyTorch provides device memory and streams.  There is no fallback: if the library
 is missing the import of an entry point raises.
 
-Entry points (same names as the C ABI): ``kda_decode_step``, ``kda_decode_multi``, ``kda_prefill_chunked``,
+Entry points (same names as the C ABI): ``kda_project_inputs``, ``kda_decode_step``, ``kda_decode_multi``,
+``kda_prefill_chunked``,
 ``kda_resume_from_slot``, ``kda_prefill_workspace_bytes``, ``kda_checkpoint_count``,
 ``kda_status_string``; the host prefix index ``kda_prefix_*`` through :class:`PrefixIndex`.
 """
@@ -67,6 +68,8 @@ def load_library(path: str | None = None):
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_decode_multi.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Params), i32, i32] + [vp] * 11
     lib.kda_decode_multi.restype = ctypes.c_int
+    lib.kda_project_inputs.argtypes = [i64, i32, i32, i32, i32] + [vp] * 10
+    lib.kda_project_inputs.restype = ctypes.c_int
     lib.kda_checkpoint_count.argtypes = [i64, i64, i64]
     lib.kda_checkpoint_count.restype = i64
     lib.kda_prefill_workspace_bytes.argtypes = [ctypes.POINTER(_Pool), i32, i64, i32]
@@ -232,6 +235,20 @@ def kda_decode_step(pool: StatePool, params: LayerParams, q, k, v, a, b, z, y, s
                                         _ptr(b), _ptr(z), _ptr(y), _ptr(src_slot), _ptr(dst_slot),
                                         _ptr(dev_status), _stream(stream))
     _check(rc, "kda_decode_step")
+
+
+def projection_width(H: int, dk: int, dv: int) -> int:
+    """Rows of the packed projection weight: q, k, v, a, z and b."""
+    return H * (3 * dk + 2 * dv) + H
+
+
+def kda_project_inputs(x, w, H: int, dk: int, dv: int, q, k, v, a, b, z, dev_status, stream=None) -> None:
+    """The six input projections in one GEMM (see include/kda.h): x [T, hidden] bf16, w [N, hidden] bf16 with
+    the rows of q, k, v, a, z, b; outputs q, k, a [T, H, dk], v, z [T, H, dv], b [T, H] bf16 (z may be None)."""
+    T, hidden = int(x.shape[0]), int(x.shape[1])
+    rc = load_library().kda_project_inputs(T, hidden, int(H), int(dk), int(dv), _ptr(x), _ptr(w), _ptr(q), _ptr(k),
+                                           _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(dev_status), _stream(stream))
+    _check(rc, "kda_project_inputs")
 
 
 DECODE_MULTI_MAX_L = 8  # KDA_DECODE_MULTI_MAX_L in kda.h

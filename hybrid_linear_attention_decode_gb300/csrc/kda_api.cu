@@ -223,6 +223,32 @@ int kda_decode_multi(const kda_pool *pool, const kda_params *prm, int32_t n, int
     return launch_decode_multi(d, pool->dk, pool->dv, L, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kda_project_inputs(int64_t T, int32_t hidden, int32_t H, int32_t dk, int32_t dv, const uint16_t *x,
+                       const uint16_t *w, uint16_t *q, uint16_t *k, uint16_t *v, uint16_t *a, uint16_t *b, uint16_t *z,
+                       int32_t *dev_status, kda_stream_t stream) {
+    clear_error();
+    if (T < 0 || hidden <= 0 || H <= 0 || dk <= 0 || dv <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "project: T must be >= 0 and hidden, H, dk, dv positive");
+    if (hidden % 8) return fail(KDA_ERR_INVALID_ARG, "project: hidden must be a multiple of 8 (16-byte rows)");
+    if (T > 0x7fffffffLL || (int64_t)H * (3 * dk + 2 * dv + 1) > 0x7fffffffLL)
+        return fail(KDA_ERR_INVALID_ARG, "project: T or the projection width too large");
+    if (T == 0) return KDA_OK;
+    if (!x || !w || !q || !k || !v || !a || !b) return fail(KDA_ERR_INVALID_ARG, "project: a required pointer is NULL");
+    if (!aligned16(x) || !aligned16(w) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) ||
+        (z && !aligned16(z)) || !aligned2(b) || (dev_status && !aligned4(dev_status)))
+        return fail(KDA_ERR_INVALID_ARG, "project: x, w, q, k, v, a, z must be 16-byte aligned, b 2-byte");
+    ProjectArgs p;
+    p.T = T;
+    p.hidden = hidden;
+    p.H = H;
+    p.dk = dk;
+    p.dv = dv;
+    p.x = x; p.w = w;
+    p.q = q; p.k = k; p.v = v; p.a = a; p.z = z; p.b = b;
+    p.status = dev_status;
+    return launch_project(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t kda_prefill_workspace_bytes(const kda_pool *pool, int32_t nseq, int64_t total_tokens, int32_t chunk) {
     if (!pool || nseq < 0 || total_tokens < 0 || pool->H <= 0) return 0;
     if (!prefill_supported(pool->dk, pool->dv, pool->conv_w, chunk)) return 0;

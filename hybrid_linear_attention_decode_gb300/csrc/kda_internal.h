@@ -65,6 +65,15 @@ int launch_decode_multi(const DecodeArgs &a, int dk, int dv, int L, cudaStream_t
 
 int launch_resume(const ResumeArgs &a, cudaStream_t st);
 
+struct ProjectArgs {
+    int64_t T;
+    int32_t hidden, H, dk, dv;
+    const uint16_t *x, *w;                 // [T][hidden], [N][hidden] bf16
+    uint16_t *q, *k, *v, *a, *z, *b;       // [T][H][dk | dv], b [T][H]; z may be NULL
+    int32_t *status;
+};
+int launch_project(const ProjectArgs &a, cudaStream_t st);
+
 bool prefill_supported(int dk, int dv, int W, int chunk);
 size_t prefill_workspace_bytes(int H, int dk, int dv, int nseq, int64_t total_tokens, int chunk);
 int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st);

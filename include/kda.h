@@ -110,6 +110,25 @@ KDA_API int kda_decode_step(const kda_pool *pool, const kda_params *prm, int32_t
                     const uint16_t *v, const uint16_t *a, const uint16_t *b, const uint16_t *z, uint16_t *y,
                     const int32_t *src_slot, const int32_t *dst_slot, int32_t *dev_status, kda_stream_t stream);
 
+/*
+ * The input projections of a KDA layer in one GEMM ("A Preview of Production-Scale Kimi K3 Support on
+ * vLLM", section "KDA prefill and decode": the input projections and the causal convolution are fused around
+ * the core recurrence).  q, k, v, the decay logits a, the output gate z and the beta logits b come from one
+ * packed weight matrix and are written in the layout kda_prefill_chunked reads; the causal convolution is
+ * fused into the prefill's chunk kernel, which consumes these raw rows.
+ *   x    device [T][hidden] bf16 hidden states (hidden % 8 == 0)
+ *   w    device [N][hidden] bf16, N = H*(3*dk + 2*dv) + H: the rows of q (H*dk), k (H*dk), v (H*dv),
+ *        a (H*dk), z (H*dv) and b (H), in that order (row = output feature, K-major)
+ *   q, k, a  device [T][H][dk] bf16 out    v, z  device [T][H][dv] bf16 out (z may be NULL: not stored)
+ *   b    device [T][H] bf16 out
+ *   dev_status device int32, OR-ed with KDA_DEV_TIMEOUT if a bounded wait gave up.
+ * fp32 accumulation in tensor memory; each output rounded to bf16 (nearest even).  All pointers but b
+ * 16-byte aligned.  Asynchronous on `stream`; allocates nothing.
+ */
+KDA_API int kda_project_inputs(int64_t T, int32_t hidden, int32_t H, int32_t dk, int32_t dv, const uint16_t *x,
+                               const uint16_t *w, uint16_t *q, uint16_t *k, uint16_t *v, uint16_t *a, uint16_t *b,
+                               uint16_t *z, int32_t *dev_status, kda_stream_t stream);
+
 /* Most tokens per request that one kda_decode_multi call takes. */
 #define KDA_DECODE_MULTI_MAX_L 8
 

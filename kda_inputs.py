@@ -107,6 +107,14 @@ def token_inputs(seed: int, T: int, H: int, dk: int, dv: int, with_z: bool = Tru
     return out
 
 
+def projection_inputs(seed: int, T: int, hidden: int, N: int, offset_tokens: int = 0) -> tuple:
+    """bf16 bit patterns of hidden states x [T, hidden] ~ N(0, 1) and a packed projection weight W [N, hidden]
+    ~ N(0, 1/hidden) (so each projected value is about N(0, 1))."""
+    x = f32_to_bf16_bits(normal(seed, STREAM["misc"] + 100, (T, hidden), offset_tokens * hidden))
+    w = f32_to_bf16_bits(normal(seed, STREAM["misc"] + 101, (N, hidden)) / np.float32(np.sqrt(hidden)))
+    return x, w
+
+
 def layer_weights(seed: int, H: int, dk: int, dv: int, W: int = 4) -> dict:
     """Per-layer constants: conv weights [H, 2dk+dv, W] and RMSNorm weight [dv], fp32."""
     Cc = 2 * dk + dv

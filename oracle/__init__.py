@@ -18,7 +18,8 @@ gcc, marshals numpy arrays, and states the slot-pool semantics of the three oper
 * resume ("The Hardest Part: Prefix Caching for KDA", copy-on-write): slot ``dst[n]`` receives a copy
   of slot ``src[n]``;
 * multi-token decode ("vLLM Kimi K3 Support", section "Speculative Decoding with DSpark"): L tokens per
-  request in order, the state after token j kept in slot ``dst_slots[r*L + j]`` unless it is -1.
+  request in order, the state after token j kept in slot ``dst_slots[r*L + j]`` unless it is -1;
+* input projections: q, k, v, a, z, b = x W^T split by rows of the packed weight.
 
 Parity unpinned by the pages: they print no worked numeric example; every pin in the test suite comes
 from algebra (closed forms, invariants, brute force, exact rational arithmetic).
@@ -210,6 +211,24 @@ def decode_pool(cfg: Cfg, pool_S, pool_conv, src_slot, dst_slot, q, k, v, a, b, 
         out_S[d] = _store(r["S"][n], state_bf16)
         out_C[d] = r["conv"][n]
     return dict(pool_S=out_S, pool_conv=out_C, o=r["o"], y=r["y"])
+
+
+def project(x, w, H: int, dk: int, dv: int) -> dict:
+    """The input projections of a layer: Y = x W^T in fp64, split by rows of W into q, k, v, a, z [T, H, d]
+    and b [T, H] ("A Preview of Production-Scale Kimi K3 Support on vLLM", section "KDA prefill and decode":
+    the input projections feeding the recurrence).  x [T, hidden], w [N, hidden], N = H*(3dk + 2dv) + H."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    y = x @ w.T
+    T = x.shape[0]
+    out, c = {}, 0
+    for name, width, d in (("q", H * dk, dk), ("k", H * dk, dk), ("v", H * dv, dv), ("a", H * dk, dk),
+                           ("z", H * dv, dv), ("b", H, 1)):
+        blk = y[:, c:c + width]
+        out[name] = blk.reshape(T, H) if name == "b" else blk.reshape(T, H, d)
+        c += width
+    assert c == w.shape[0]
+    return out
 
 
 def decode_multi_pool(cfg: Cfg, pool_S, pool_conv, L: int, src_slot, dst_slots, q, k, v, a, b, z, conv_w, norm_w,

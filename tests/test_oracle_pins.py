@@ -426,3 +426,24 @@ def test_multi_token_decode_equals_chained_single_steps():
                                   tok["v"], tok["a"], tok["b"], tok["z"], conv_w, norm_w, state_bf16=True)
     np.testing.assert_array_equal(rb["y"], r["y"])
     np.testing.assert_array_equal(rb["pool_S"][8], oracle.round_to_bf16(r["pool_S"][8]))
+
+
+def test_projection_definition_by_explicit_loops():
+    """oracle.project against explicit sums on a tiny case: the row order of the packed weight (q, k, v, a,
+    z, b) and the [T, H, d] split of each block."""
+    H, dk, dv, hidden, T = 2, 3, 2, 5, 4
+    rng = np.random.default_rng(5)
+    N = H * (3 * dk + 2 * dv) + H
+    x = rng.standard_normal((T, hidden))
+    w = rng.standard_normal((N, hidden))
+    got = oracle.project(x, w, H, dk, dv)
+    row = 0
+    for name, d in (("q", dk), ("k", dk), ("v", dv), ("a", dk), ("z", dv), ("b", None)):
+        for h in range(H):
+            for c in range(d or 1):
+                for t in range(T):
+                    want = sum(x[t, i] * w[row, i] for i in range(hidden))
+                    val = got[name][t, h] if d is None else got[name][t, h, c]
+                    assert abs(val - want) <= 1e-12 * (1 + abs(want)), (name, h, c, t)
+                row += 1
+    assert row == N
