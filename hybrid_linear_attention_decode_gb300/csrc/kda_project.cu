@@ -6,12 +6,14 @@
 // kernel, which reads these raw rows anyway, so the path has no separate conv pass.
 //
 // Design (sm_103a):
-//   * one CTA of 4 warps per 128 x 256 output tile; K in steps of 64 bf16 (one 128-byte swizzle atom);
+//   * persistent: one CTA of 6 warps per SM walks 128 x 256 output tiles; K in steps of 64 bf16 (one
+//     128-byte swizzle atom);
 //   * a 4-stage pipeline of 2-D TMA tensor loads (128B swizzle, the K-major layout the MMA descriptors
 //     read), with full / empty mbarriers; warp 0 produces, warp 1 issues tcgen05.mma (M 128, N 256, K 16)
-//     into a 128 x 256 fp32 accumulator in tensor memory and commits each stage back to its producer;
-//   * the epilogue (all 4 warps, one token row per thread) reads the accumulator with tcgen05.ld, rounds to
-//     bf16 and stores 16-byte groups into the projection each column belongs to;
+//     and commits each stage back to the producer;
+//   * two 128 x 256 fp32 accumulators in tensor memory (512 columns): while the MMAs fill one, the
+//     epilogue warps 2..5 (one lane quadrant, i.e. 32 token rows, each) read the other with tcgen05.ld,
+//     round to bf16 and store 16-byte groups into the projection each column belongs to;
 //   * tiles are rastered in groups of 16 M-tiles, so the weight tiles in flight stay in L2 while every
 //     token tile of the group uses them.
 // Every wait is bounded; a wait that gives up sets KDA_DEV_TIMEOUT and the tile is not stored.
@@ -27,7 +29,7 @@
 namespace kda {
 namespace proj {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, NT = 128, GM = 16;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, NT = 192, GM = 16;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -75,85 +77,127 @@ __device__ __forceinline__ void store8(const Args &p, int64_t row, int n, const 
     }
 }
 
+// Tile `t` of the raster: groups of GM M-tiles, M fastest inside a group.
+__device__ __forceinline__ void tile_coords(const Args &p, int t, int &tm, int &tn) {
+    const int per_group = GM * p.ntn;
+    const int g = t / per_group, rem = t - g * per_group;
+    const int gm0 = g * GM, gsz = min(GM, p.ntm - gm0);
+    tm = gm0 + rem % gsz;
+    tn = rem / gsz;
+}
+
 __global__ void __launch_bounds__(NT, 1)
     kda_project_kernel(const Args p, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + OFF_BAR);  // [STAGES] stage loaded
     uint64_t *empty = full + STAGES;                               // [STAGES] stage consumed by the MMAs
-    uint64_t *done = empty + STAGES;                               // accumulator complete
-    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *acc_full = empty + STAGES;                           // [2] accumulator complete
+    uint64_t *acc_empty = acc_full + 2;                            // [2] accumulator read by the epilogue
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(acc_empty + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // raster: groups of GM M-tiles, M fastest inside a group
-    const int per_group = GM * p.ntn;
-    const int g = blockIdx.x / per_group, rem = blockIdx.x - g * per_group;
-    const int gm0 = g * GM, gsz = min(GM, p.ntm - gm0);
-    const int tm = gm0 + rem % gsz, tn = rem / gsz;
+    const int ntiles = p.ntm * p.ntn;
     const int nk = (p.hidden + BK - 1) / BK;
 
-    if (warp == 0) umma::alloc(tmem_s, BN);
+    if (warp == 0) umma::alloc(tmem_s, 2 * BN);
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
-        mbar_init(done, 1);
+        for (int a2 = 0; a2 < 2; ++a2) {
+            mbar_init(acc_full + a2, 1);
+            mbar_init(acc_empty + a2, 4);  // one arrival per epilogue warp
+        }
         fence_mbar_init();
     }
     umma::fence_before();
     __syncthreads();
     umma::fence_after();
     const uint32_t tmem = *tmem_s;
+    bool ok = true;
 
-    if (warp == 0 && lane == 0) {  // producer: TMA loads of the x and W tiles of each K step
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % STAGES;
-            if (kb >= STAGES && !mbar_wait(empty + s, (uint32_t)(kb / STAGES - 1) & 1u)) break;
-            uint8_t *sa = sm + s * STAGE_BYTES;
-            mbar_arrive_expect_tx(full + s, STAGE_BYTES);
-            tma_load_2d(sa, &tm_x, kb * BK, tm * BM, full + s);
-            tma_load_2d(sa + A_BYTES, &tm_w, kb * BK, tn * BN, full + s);
+    if (warp == 0) {
+        if (lane == 0) {  // producer: TMA loads of the x and W tiles of every K step of every tile
+            int kg = 0;   // K steps issued so far (all tiles): stage kg % STAGES, use kg / STAGES
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(p, t, tm, tn);
+                for (int kb = 0; kb < nk; ++kb, ++kg) {
+                    const int s = kg % STAGES;
+                    if (kg >= STAGES && !mbar_wait(empty + s, (uint32_t)(kg / STAGES - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = sm + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(full + s, STAGE_BYTES);
+                    tma_load_2d(sa, &tm_x, kb * BK, tm * BM, full + s);
+                    tma_load_2d(sa + A_BYTES, &tm_w, kb * BK, tn * BN, full + s);
+                }
+            }
         }
-    } else if (warp == 1 && lane == 0) {  // MMA issuer
-        const uint32_t id = umma::idesc(umma::kBF16, BM, BN);
-        bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % STAGES;
-            if (!mbar_wait(full + s, (uint32_t)(kb / STAGES) & 1u)) {
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMA issuer: accumulator i % 2 for the i-th tile of this CTA
+            const uint32_t id = umma::idesc(umma::kBF16, BM, BN);
+            int kg = 0, i = 0;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+                const int a2 = i & 1;
+                if (i >= 2 && !mbar_wait(acc_empty + a2, (uint32_t)(i / 2 - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                umma::fence_after();
+                const uint32_t acc = tmem + (uint32_t)(a2 * BN);
+                for (int kb = 0; kb < nk; ++kb, ++kg) {
+                    const int s = kg % STAGES;
+                    if (!mbar_wait(full + s, (uint32_t)(kg / STAGES) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    umma::fence_after();
+                    const uint8_t *sa = sm + s * STAGE_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks)
+                        umma::mma_bf16(acc, umma::sdesc_k(sa, BM, ks), umma::sdesc_k(sa + A_BYTES, BN, ks), id,
+                                       kb > 0 || ks > 0);
+                    umma::commit(empty + s);  // the stage is free once these MMAs have read it
+                }
+                if (ok) umma::commit(acc_full + a2);
+            }
+        }
+    } else if (warp < 6) {  // epilogue warps 2..5: tensor-memory lane quadrant warp % 4 = rows of the tile
+        const int quad = warp & 3;
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int a2 = i & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(acc_full + a2, (uint32_t)(i / 2) & 1u))) {
                 ok = false;
                 break;
             }
             umma::fence_after();
-            const uint8_t *sa = sm + s * STAGE_BYTES;
+            int tm, tn;
+            tile_coords(p, t, tm, tn);
+            const int64_t row = (int64_t)tm * BM + quad * 32 + lane;
+            const uint32_t acc = tmem + (uint32_t)(a2 * BN) + ((uint32_t)(32 * quad) << 16);
+            for (int cg = 0; cg < BN / 32; ++cg) {
+                float v[32];
+                umma::ld32(acc + 32 * cg, v);
+                const int n0 = tn * BN + 32 * cg;
+                if (row < p.T && n0 < p.N) {
 #pragma unroll
-            for (int ks = 0; ks < BK / 16; ++ks)
-                umma::mma_bf16(tmem, umma::sdesc_k(sa, BM, ks), umma::sdesc_k(sa + A_BYTES, BN, ks), id,
-                               kb > 0 || ks > 0);
-            umma::commit(empty + s);  // the stage is free once these MMAs have read it
-        }
-        if (ok) umma::commit(done);
-    }
-    // epilogue: every thread, one token row; an accumulator that never completes is not stored
-    const bool ok = __syncthreads_or(!mbar_wait(done, 0)) == 0;
-    umma::fence_after();
-    if (ok) {
-        const int64_t row = (int64_t)tm * BM + warp * 32 + lane;  // tensor-memory lane = row of the tile
-        for (int cg = 0; cg < BN / 32; ++cg) {
-            float v[32];
-            umma::ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * cg, v);
-            const int n0 = tn * BN + 32 * cg;
-            if (row < p.T && n0 < p.N) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (n0 + 8 * j < p.N) store8(p, row, n0 + 8 * j, v + 8 * j);
+                    for (int j = 0; j < 4; ++j)
+                        if (n0 + 8 * j < p.N) store8(p, row, n0 + 8 * j, v + 8 * j);
+                }
             }
+            umma::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(acc_empty + a2, 0);  // this quadrant of the accumulator is read
         }
-    } else if (tid == 0) {
-        set_status(p.status, KDA_DEV_TIMEOUT);
     }
+    if (!ok && lane == 0) set_status(p.status, KDA_DEV_TIMEOUT);
     umma::fence_before();
     __syncthreads();
-    if (warp == 0) umma::dealloc(tmem, BN);
+    if (warp == 0) umma::dealloc(tmem, 2 * BN);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -220,7 +264,8 @@ int launch_project(const ProjectArgs &a, cudaStream_t st) {
     CUtensorMap tx, tw;
     if (!kmajor_map(enc, &tx, a.x, a.hidden, a.T, BM) || !kmajor_map(enc, &tw, a.w, a.hidden, p.N, BN))
         return fail(KDA_ERR_CUDA, "project: tensor map encoding failed");
-    kda_project_kernel<<<(unsigned)(ntm * ntn), NT, SMEM, st>>>(p, tx, tw);
+    const unsigned grid = (unsigned)std::min<int64_t>(ntm * ntn, current_device_sms());  // persistent: one per SM
+    kda_project_kernel<<<grid, NT, SMEM, st>>>(p, tx, tw);
     return launch_result("kda_project_kernel launch");
 }
 
