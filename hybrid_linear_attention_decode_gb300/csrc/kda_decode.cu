@@ -22,9 +22,11 @@
 
 namespace kda {
 
-// Resident CTAs per SM targeted for a bf16 pool at dk = dv = 128 (the register budget follows from it).
+// Resident CTAs per SM targeted for a bf16 pool at dk = dv = 128 (the register budget, 64 per thread,
+// follows from it).  Swept on the decode workload: 4 x 1 buffer 27.8 us, 3 x 1 29.2, 2 x 1 34.2, 2 x 2 35.5,
+// 3 x 2 35.4 (us per step).
 #ifndef KDA_DECODE_BF16_CTAS
-#define KDA_DECODE_BF16_CTAS 3
+#define KDA_DECODE_BF16_CTAS 4
 #endif
 #ifndef KDA_DECODE_NBUF_BF16
 #define KDA_DECODE_NBUF_BF16 1
