@@ -405,6 +405,9 @@ def run_gpu(args):
     # ---- the input projections feeding the prefill workload
     projection = run_project(args, kda, torch, dev, stream, seed, ws)
 
+    # ---- the long-context workload (prefill of one 131072-token sequence, then decode at batch 256)
+    long_context = run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
+
     # ---- chunked prefill workload
     prefill = run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
 
@@ -431,7 +434,8 @@ def run_gpu(args):
             "decode_bf16_state": decode_bf16,
             "decode_multi_verify": decode_multi,
             "projection": projection,
-            "prefill": prefill}
+            "prefill": prefill,
+            "long_context": long_context}
     if rank == 0:
         if ws == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_decode_rate(args.cpu_seconds)
@@ -580,6 +584,86 @@ def run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws):
             "tokens_per_s": DEC_N * ws / (ms / 1000.0), "ms_per_step": ms, "steps": K,
             "algorithmic_bytes_per_launch": per_ht * DEC_N * H, "achieved_gbs": gbs, "hbm_frac": gbs / hbm_peak,
             "traffic": profiled_traffic("kda_decode_bf16", sha)}
+
+
+LONG_T, LONG_INTERVAL, LONG_DEC_N = 131072, 32768, 256
+
+
+def run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
+    """The long-context workload: one 131072-token prefill (H=32, d=128, chunk 64, checkpoints every 32768
+    tokens) into the pool, then a batch-256 decode step in which request 0 continues that sequence from its
+    final state and 255 requests use other random slots.  Token inputs are drawn on the device (seeded torch
+    generator, the distributions of the other workloads); 5 GB of them would be slow to draw on the host."""
+    T, C, I = LONG_T, PRE_CHUNK, LONG_INTERVAL
+    ns = int(pool.S.shape[0])
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed + 11)
+
+    def draw(*shape, shift=0.0):
+        return (torch.randn(*shape, generator=g, device=dev) + shift).to(torch.bfloat16)
+    q, k, v, z = draw(T, H, DK), draw(T, H, DK), draw(T, H, DV), draw(T, H, DV)
+    a, b = draw(T, H, DK, shift=3.0), draw(T, H)
+    y = torch.empty(T, H, DV, dtype=torch.bfloat16, device=dev)
+    perm = torch.randperm(ns, generator=g, device=dev).to(torch.int32)
+    nck = T // I
+    dst = perm[:1].contiguous()
+    ck = perm[1:1 + nck].contiguous()
+    i32 = lambda x: torch.tensor(x, dtype=torch.int32, device=dev)  # noqa: E731
+    cu, offs, src = i32([0, T]), i32([0, nck]), i32([-1])
+    sp = torch.zeros(1, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_buf = torch.empty(kda.kda_prefill_workspace_bytes(pool, 1, T, C), dtype=torch.uint8, device=dev)
+
+    def pre():
+        kda.kda_prefill_chunked(pool, prm, cu, sp, src, dst, C, I, offs, ck, q, k, v, a, b, z, y, ws_buf, status,
+                                stream)
+    pre()
+    torch.cuda.synchronize()
+    barrier(ws)
+    Kp = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Kp):
+        pre()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pre_ms = max_over_ranks(e0.elapsed_time(e1), ws) / Kp
+    del ws_buf, q, k, v, a, z, b, y
+    # decode at batch 256: request 0 continues the long sequence (in place), the rest use other slots
+    N = LONG_DEC_N
+    others = perm[1 + nck:1 + nck + N - 1]
+    slots = torch.cat([dst, others]).contiguous()
+    dq, dk_, dv_, dz = draw(N, H, DK), draw(N, H, DK), draw(N, H, DV), draw(N, H, DV)
+    da, db = draw(N, H, DK, shift=3.0), draw(N, H)
+    yd = torch.empty(N, H, DV, dtype=torch.bfloat16, device=dev)
+    Kd = 200
+
+    def dec(st_=None):
+        kda.kda_decode_step(pool, prm, dq, dk_, dv_, da, db, dz, yd, slots, slots, status, st_)
+    for _ in range(3):
+        dec(stream)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        for _ in range(Kd):
+            dec()
+    gr.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0.record(stream)
+    gr.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = max_over_ranks(e0.elapsed_time(e1), ws) / Kd
+    del gr
+    if int(status.item()) != 0:
+        return {"error": f"device status {int(status.item())}"}
+    dec_bytes = DECODE_BYTES_PER_HEAD_TOKEN * N * H
+    return {"workload": f"long context: one {T}-token prefill (H=32, d=128, chunk 64, checkpoints every {I} "
+                        f"tokens), then a batch-{N} decode step continuing it plus {N - 1} other slots",
+            "prefill_ms": pre_ms, "prefill_tokens_per_s": T * ws / (pre_ms / 1000.0),
+            "decode_us": dec_ms * 1000.0, "decode_tokens_per_s": N * ws / (dec_ms / 1000.0),
+            "decode_hbm_frac": dec_bytes / (dec_ms / 1000.0) / 1e9 / hbm_peak}
 
 
 def prefill_problem(seed: int, lens, chunk: int, interval: int, num_slots: int):
