@@ -1232,21 +1232,24 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                     umma::mma_bf16(tmem + T_O, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_QP, CH, ks), idp, ks > 0);
             }
             ph_w ^= 1;
+            // each thread waits for U^T itself; a timed-out wait is voted on at the barrier after the U tiles
             ok = mbar_wait(bar_mma, ph_m);
             ph_m ^= 1;
-            ok = !state_sync_or(!ok);
             umma::fence_after();
-            if (!ok) break;
-            if (tid == 0 && has_next) issue_w(c + 1);  // the U^T MMAs no longer read -W
+            if (tid == 0 && ok && has_next) issue_w(c + 1);  // the U^T MMAs no longer read -W
             // ---- U = U' + U^T -> its tf32 and bf16 operand tiles ----
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_u, ph_u));  // warp-uniform: ld32 is a warp operation
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_u, ph_u) && ok);  // warp-uniform: the load is a warp operation
             ph_u ^= 1;
             if (ok) {
-                float v[32];
-                umma::ld32(tmem + lane_off + T_U + 32 * half, v);
                 const float *up = reinterpret_cast<const float *>(ops + WS_UP);
+                float v[32];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] += up[(32 * half + t) * D + j];
+                for (int t = 0; t < 32; ++t) v[t] = up[(32 * half + t) * D + j];  // in flight with the U^T load
+                uint32_t r[32];
+                umma::ld32_issue(tmem + lane_off + T_U + 32 * half, r);
+                umma::wait_ld(r);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] += __uint_as_float(r[t]);
 #pragma unroll
                 for (int t = 0; t < 32; t += 4)
                     umma::st_tf32x4(Ut32, D, j, 32 * half + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
@@ -1277,18 +1280,24 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 }
             }
             ph_b ^= 1;
-            ok = mbar_wait(bar_mma, ph_m);
+            // each thread waits for S^T itself; the vote is taken at the end of the chunk
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_m));
             ph_m ^= 1;
-            ok = !state_sync_or(!ok);
             umma::fence_after();
-            if (!ok) break;
-            if (tid == 0 && has_next) issue_qp(c + 1);  // every MMA before the S^T commit is done: Q+ is free
-            // ---- S pass: bf16 tile of the new state, checkpoint, then decay by the next chunk (or the final store)
-            {
-                float v[32];
-                for (int part = 0; part < 2; ++part) {
-                    const int i0 = 64 * half + 32 * part;
-                    umma::ld32(tmem + lane_off + T_S + i0, v);
+            if (tid == 0 && ok && has_next) issue_qp(c + 1);  // every MMA before the S^T commit is done: Q+ is free
+            // ---- S pass: bf16 tile of the new state, checkpoint, then decay by the next chunk (or the final
+            //      store); both halves of this thread's columns are loaded at once and stored back together ----
+            if (ok) {
+                uint32_t ra[32], rb[32];
+                const int ia = 64 * half, ib = ia + 32;
+                umma::ld32_issue(tmem + lane_off + T_S + ia, ra);
+                umma::ld32_issue(tmem + lane_off + T_S + ib, rb);
+                umma::wait_ld(ra);
+                umma::wait_ld(rb);
+                auto s_part = [&](uint32_t *r, int i0) {
+                    float v[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
                     if (ck >= 0) {
 #pragma unroll
                         for (int t = 0; t < 32; ++t)
@@ -1299,21 +1308,24 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                         for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
 #pragma unroll
                         for (int t = 0; t < 32; ++t) v[t] *= gln[i0 + t];
-                        umma::st32(tmem + lane_off + T_S + i0, v);
+                        umma::st32_issue(tmem + lane_off + T_S + i0, v);
                     } else {
 #pragma unroll
                         for (int t = 0; t < 32; ++t)
                             store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
                     }
-                }
+                };
+                s_part(ra, ia);
+                s_part(rb, ib);
+                umma::wait_st();
             }
             // ---- O^T -> the staging buffer of the output warps (once they have consumed the previous one) ----
-            if (c > c0) ok = __all_sync(0xffffffffu, mbar_wait(bar_empty, (uint32_t)(c - c0 - 1) & 1u));
+            if (c > c0) ok = __all_sync(0xffffffffu, mbar_wait(bar_empty, (uint32_t)(c - c0 - 1) & 1u) && ok);
             ok = __all_sync(0xffffffffu, mbar_wait(bar_o, ph_o) && ok);
             ph_o ^= 1;
             umma::fence_after();
             if (tid == 0 && ok && has_next) issue_b(c + 1);  // every MMA of this chunk is done: Qk, Ktil^T free
-            {
+            if (ok) {
                 float v[32];
                 umma::ld32(tmem + lane_off + T_O + 32 * half, v);
 #pragma unroll
