@@ -517,20 +517,22 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 //   P0-P1  [0,32K) q^ fp32 | [32K,64K) k^ fp32 | [64K,96K) G fp32 (decay logits staged in its first 16K) |
 //          [96K,128K) V^T tf32 tile | [128K,180K) raw rows
 //   P2     [128K,160K) [K+;Q+] bf16 tile | [160K,176K) K- bf16 tile
-//   P3-P4  [0,8K) Qk staging, then [0,16K) Inv fp32 | [128K,145K) A fp32 (row stride 68) | [160K,176K) block temps,
+//   P3-P4  [0,8K) Qk staging, then [0,17K) Inv fp32 (row stride 68) | [128K,145K) A fp32 (row stride 68) | [160K,176K) block temps,
 //          then T tf32
 //   P5     [0,32K) (k exp G)^T tf32 tile | [128K,160K) Ktil^T tf32 staging
 //   P6     [32K,48K) -W bf16 staging | [64K,96K) U' fp32 staging
 constexpr uint32_t I_Q = 0, I_K = 32768, I_G = 65536, I_VT = 98304, I_RAW = 131072;
 constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_T = 163840;
-constexpr uint32_t I_INV = 0;          // Inv fp32 [64][64] over q^ (free after the Qk copy-out)
+constexpr uint32_t I_INV = 0;          // Inv fp32 [64][IST] over q^ (free after the Qk copy-out)
 constexpr uint32_t I_QKS_SLOW = 148480; // Qk staging of the wide-decay path (q^ is still read there)
 constexpr uint32_t I_MISC = 184320;   // beta, exp(G_mid), decay partial sums, barrier, tmem address, window stash
 constexpr uint32_t I_SMEM = I_MISC + 7168 + 1024;  // + alignment slack
 constexpr int RAW_ROWS = CH + kConvW - 1;           // 3 history rows + 64 tokens
 constexpr int AST = 68;                             // row stride of A in smem (padded against bank conflicts)
+constexpr int IST = 68;                             // row stride of Inv in smem (the same padding)
 static_assert(I_A + CH * AST * 4 <= I_QKS_SLOW && I_QKS_SLOW + CH * CH * 2 <= I_T, "A and slow Qk staging");
 static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
+static_assert(I_INV + CH * IST * 4 <= I_K && (IST * 4) % 16 == 0, "Inv staging");
 
 constexpr int NTI = 512;  // intra kernel threads
 constexpr int RAW_PART = RAW_ROWS * D;  // elements of one raw block ([67][128] bf16 of q, k or v)
@@ -825,7 +827,7 @@ __global__ void __launch_bounds__(NTI, 1)
     }
     // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with diagonal, bf16 tile) ----
     float *A = reinterpret_cast<float *>(sm + I_A);      // [64][AST]
-    float *Inv = reinterpret_cast<float *>(sm + I_INV);  // [64][64]
+    float *Inv = reinterpret_cast<float *>(sm + I_INV);  // [64][IST], lower block triangle
     // Qk tile staging: over q^ (dead) on the fast path; the slow path still reads q^, so it stages behind A
     uint8_t *Qks = slow ? sm + I_QKS_SLOW : sm + I_Q;
     if (ok && !slow) {
@@ -883,7 +885,8 @@ __global__ void __launch_bounds__(NTI, 1)
     }
     __syncthreads();
     // ---- P4: T = (I + diag(beta) A)^{-1} diag(beta), blocked by 16 ----
-    // L = I + diag(beta) A; Inv = L^{-1}.  Diagonal 16x16 blocks by substitution, one column per thread.
+    // L = I + diag(beta) A; Inv = L^{-1}, of which only the lower block triangle is formed (the blocks above
+    // the diagonal are zero).  Diagonal 16x16 blocks by substitution, one column per thread.
     if (tid < CH) {
         const int b = tid >> 4, col = tid & 15, base = 16 * b;
         float x[16];
@@ -896,41 +899,57 @@ __global__ void __launch_bounds__(NTI, 1)
             x[r] = acc;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Inv[(base + r) * CH + base + col] = x[r];
-    }
-    for (int idx = tid; idx < CH * CH; idx += NTI) {
-        const int r = idx / CH, s_ = idx - (idx / CH) * CH;
-        if ((s_ >> 4) > (r >> 4)) Inv[idx] = 0.f;
+        for (int r = 0; r < 16; ++r) Inv[(base + r) * IST + base + col] = x[r];
     }
     __syncthreads();
+    // Off-diagonal blocks (i, j = i - d) by distance d:  P_i = diag(beta_i) sum_{k=j}^{i-1} A_ik Inv_kj, then
+    // Inv_ij = -Inv_ii P_i.  Each thread forms one row and four columns of a block; a warp covers 8 rows x 16
+    // columns, so the row-stride-68 reads of A and Inv_ii fall in distinct banks.
     float *P = reinterpret_cast<float *>(sm + I_T);  // [3][16][16] temporaries (K- is dead)
     for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;  // blocks (i, i-d) for i = d..3
-        for (int idx = tid; idx < nb * 256; idx += NTI) {  // P_i = sum_{k=i-d}^{i-1} L_ik Inv_k,(i-d)
-            const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
-            const int i = bi + d, j = i - d;
-            float acc = 0.f;
-            for (int k = j; k < i; ++k)
+        const bool act = tid < nb * 64;
+        const int bi = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        const int i = bi + d, j = i - d;
+        if (act) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = j; k < i; ++k) {
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    acc = fmaf(A[(16 * i + rr) * AST + 16 * k + t], Inv[(16 * k + t) * CH + 16 * j + cc], acc);
-            P[idx] = beta[16 * i + rr] * acc;
+                for (int t = 0; t < 16; ++t) {
+                    const float av = A[(16 * i + rr) * AST + 16 * k + t];
+                    const float4 iv = *reinterpret_cast<const float4 *>(Inv + (16 * k + t) * IST + 16 * j + c4);
+                    acc.x = fmaf(av, iv.x, acc.x);
+                    acc.y = fmaf(av, iv.y, acc.y);
+                    acc.z = fmaf(av, iv.z, acc.z);
+                    acc.w = fmaf(av, iv.w, acc.w);
+                }
+            }
+            const float br = beta[16 * i + rr];
+            *reinterpret_cast<float4 *>(P + bi * 256 + rr * 16 + c4) =
+                make_float4(br * acc.x, br * acc.y, br * acc.z, br * acc.w);
         }
         __syncthreads();
-        for (int idx = tid; idx < nb * 256; idx += NTI) {  // Inv_ij = -Inv_ii P_i
-            const int bi = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
-            const int i = bi + d, j = i - d;
-            float acc = 0.f;
+        if (act) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) acc = fmaf(Inv[(16 * i + rr) * CH + 16 * i + t], P[bi * 256 + t * 16 + cc], acc);
-            Inv[(16 * i + rr) * CH + 16 * j + cc] = -acc;
+            for (int t = 0; t < 16; ++t) {
+                const float lv = Inv[(16 * i + rr) * IST + 16 * i + t];
+                const float4 pv = *reinterpret_cast<const float4 *>(P + bi * 256 + t * 16 + c4);
+                acc.x = fmaf(lv, pv.x, acc.x);
+                acc.y = fmaf(lv, pv.y, acc.y);
+                acc.z = fmaf(lv, pv.z, acc.z);
+                acc.w = fmaf(lv, pv.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(Inv + (16 * i + rr) * IST + 16 * j + c4) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
     }
     uint8_t *Tt = sm + I_T;  // T tf32 [64 r][64 s]: the B operand of W^T = K+^T T^T (K-major: row r, K = s)
     for (int idx = tid; idx < CH * 16; idx += NTI) {
         const int r = idx >> 4, s0 = (idx & 15) * 4;
-        const float4 iv = *reinterpret_cast<const float4 *>(Inv + r * CH + s0);
+        const float4 iv = (s0 >> 4) > (r >> 4) ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                               : *reinterpret_cast<const float4 *>(Inv + r * IST + s0);
         umma::st_tf32x4(Tt, CH, r, s0, iv.x * beta[s0], iv.y * beta[s0 + 1], iv.z * beta[s0 + 2], iv.w * beta[s0 + 3]);
     }
     __syncthreads();  // A / Inv are dead: Ktil^T may be staged over them
