@@ -906,6 +906,7 @@ __global__ void __launch_bounds__(NTI, 1)
     // Inv_ij = -Inv_ii P_i.  Each thread forms one row and four columns of a block; a warp covers 8 rows x 16
     // columns, so the row-stride-68 reads of A and Inv_ii fall in distinct banks.
     float *P = reinterpret_cast<float *>(sm + I_T);  // [3][16][16] temporaries (K- is dead)
+#pragma unroll
     for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;  // blocks (i, i-d) for i = d..3
         const bool act = tid < nb * 64;
@@ -913,7 +914,9 @@ __global__ void __launch_bounds__(NTI, 1)
         const int i = bi + d, j = i - d;
         if (act) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int k = j; k < i; ++k) {
+#pragma unroll
+            for (int kk = 0; kk < d; ++kk) {
+                const int k = j + kk;
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const float av = A[(16 * i + rr) * AST + 16 * k + t];
