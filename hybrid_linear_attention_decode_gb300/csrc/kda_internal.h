@@ -56,6 +56,9 @@ struct PrefillArgs {
     void *ws;
     size_t ws_bytes;
     int32_t *status;
+    // Range [seg_lo, seg_hi) of the call's chunks (numbered over all sequences) that one launch of the
+    // tensor-core kernels processes; the whole call unless the launcher splits it into segments.
+    int32_t seg_lo = 0, seg_hi = INT32_MAX;
 };
 
 bool decode_supported(int dk, int dv, int W);

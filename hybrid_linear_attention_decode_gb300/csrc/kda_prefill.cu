@@ -24,6 +24,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__(kThreads) prefill_out_kernel(const PrefillArgs
 // tf32 operands are rounded to nearest (cvt.rna); accumulation is fp32 in tensor memory.
 namespace tc {
 
-constexpr int D = 128, CH = 64, NT = 256;
+constexpr int D = 128, CH = 64;
 constexpr float kMidRange = 40.f;  // |G_r - G_mid| bound for the factorised A / Qk (fp32-safe)
 
 // Workspace block per (chunk, head); the first WS_OPS bytes are operand tiles in their shared-memory
@@ -482,7 +483,7 @@ static_assert(WS_OPS % 16 == 0, "bulk copy size");
 
 struct Layout2 {
     int64_t maxc;
-    size_t off_cnt, off_ent, off_pos, off_seqc, off_flags, off_blk, total;
+    size_t off_cnt, off_ent, off_pos, off_seqc, off_flags, off_blk, off_carry, total;
 };
 
 inline Layout2 make_layout2(int H, int nseq, int64_t T) {
@@ -496,6 +497,7 @@ inline Layout2 make_layout2(int H, int nseq, int64_t T) {
     L.off_flags = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
     o = (o + 1023) & ~size_t(1023);
     L.off_blk = o; o += (size_t)WS_BLOCK * L.maxc * H;
+    L.off_carry = o; o += (size_t)nseq * H * D * D * 4;  // fp32 state of each (sequence, head) between segments
     L.total = o;
     return L;
 }
@@ -570,8 +572,10 @@ __global__ void __launch_bounds__(NTI, 1)
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, CC = 3 * D;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int total = *wsp<int32_t>(a, L.off_cnt) * H;  // work items (chunk, head), head fastest
-    if ((int)blockIdx.x >= total) return;
+    // work items (chunk, head), head fastest: those of the chunks [seg_lo, seg_hi)
+    const int item_lo = a.seg_lo * H;
+    const int total = min(*wsp<int32_t>(a, L.off_cnt), a.seg_hi) * H;
+    if (item_lo + (int)blockIdx.x >= total) return;
 
     float *qh = reinterpret_cast<float *>(sm + I_Q);
     float *kh = reinterpret_cast<float *>(sm + I_K);
@@ -618,19 +622,20 @@ __global__ void __launch_bounds__(NTI, 1)
         mbar_init(bar, 1);
         mbar_init(bar_in, 1);
         fence_mbar_init();
-        load_meta(blockIdx.x, &meta[0]);
-        issue_rows(meta[0], (int)blockIdx.x % H);
-        issue_logits(meta[0], (int)blockIdx.x % H);
+        load_meta(item_lo + blockIdx.x, &meta[0]);
+        issue_rows(meta[0], (item_lo + (int)blockIdx.x) % H);
+        issue_logits(meta[0], (item_lo + (int)blockIdx.x) % H);
     }
     __syncthreads();  // barriers, the tensor-memory address and the first item's metadata are in place
     const uint32_t tmem = *tmem_s;
     uint32_t phase = 0, ph_in = 0;
     bool ok = true, in_flight = true;  // in_flight: row loads issued and not yet waited for (thread 0's view)
     // the first item's beta logit; later items get theirs prefetched by the item before
-    uint16_t blogit = (tid < CH && tid < meta[0].n) ? a.b[(size_t)(meta[0].t0 + tid) * H + (int)blockIdx.x % H]
-                                                     : (uint16_t)0;
+    uint16_t blogit = (tid < CH && tid < meta[0].n)
+                          ? a.b[(size_t)(meta[0].t0 + tid) * H + (item_lo + (int)blockIdx.x) % H]
+                          : (uint16_t)0;
 
-    for (int item = blockIdx.x, it = 0; item < total; item += gridDim.x, ++it) {
+    for (int item = item_lo + blockIdx.x, it = 0; item < total; item += gridDim.x, ++it) {
     const int c = item / H, h = item - (item / H) * H;
     const int next = item + gridDim.x;
     const bool has_next = next < total;
@@ -1137,6 +1142,15 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
     const int64_t start = a.start_pos[n];
     const int32_t c0 = wsp<int32_t>(a, L.off_seqc)[n], c1 = wsp<int32_t>(a, L.off_seqc)[n + 1];
+    // this launch's chunks of the sequence: [cb, ce) = [c0, c1) within [seg_lo, seg_hi).  The state enters
+    // from the source slot at the sequence's first chunk, else from the carry written by the launch before;
+    // it leaves to the destination slot at the last chunk, else to the carry.  An empty sequence passes its
+    // state and window through in the launch of the first segment.
+    const bool empty = c0 == c1;
+    const int32_t cb = max(c0, a.seg_lo), ce = min(c1, a.seg_hi);
+    if (empty ? a.seg_lo != 0 : cb >= ce) return;
+    const bool first = cb == c0, last = ce == c1;
+    float *carry = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.ws) + L.off_carry) + ((size_t)n * H + h) * D * D;
     const ChunkEnt *ent = wsp<ChunkEnt>(a, L.off_ent);
     const int64_t *pos = wsp<int64_t>(a, L.off_pos);
     const uint8_t *blk0 = reinterpret_cast<const uint8_t *>(a.ws) + L.off_blk;
@@ -1166,11 +1180,11 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         mbar_init(bar_full, 8);
         mbar_init(bar_empty, 4);
         fence_mbar_init();
-        if (c0 < c1) {
-            issue_w(c0);
-            issue_qp(c0);
-            issue_u(c0);
-            issue_b(c0);
+        if (!empty) {
+            issue_w(cb);
+            issue_qp(cb);
+            issue_u(cb);
+            issue_b(cb);
         }
     }
     umma::fence_before();
@@ -1185,14 +1199,20 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
         // initial state: its bf16 operand tile, and S^T diag(exp(G_last of the first chunk)) in tensor memory
         {
-            const float *gl0 = c0 < c1 ? reinterpret_cast<const float *>(blk_of(c0) + WS_GL) : nullptr;
+            const float *gl0 = !empty ? reinterpret_cast<const float *>(blk_of(cb) + WS_GL) : nullptr;
             float v[32];
             for (int part = 0; part < 2; ++part) {
                 const int i0 = 64 * half + 32 * part;
+                if (first) {
 #pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    v[t] = src >= 0 ? load_state(a.S, a.state_bf16, (((size_t)src * H + h) * D + i0 + t) * D + j) : 0.f;
-                if (c0 == c1) {  // empty sequence: the state and window pass through unchanged
+                    for (int t = 0; t < 32; ++t)
+                        v[t] = src >= 0 ? load_state(a.S, a.state_bf16, (((size_t)src * H + h) * D + i0 + t) * D + j)
+                                        : 0.f;
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) v[t] = carry[(size_t)(i0 + t) * D + j];
+                }
+                if (empty) {  // empty sequence: the state and window pass through unchanged
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
                         store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
@@ -1204,7 +1224,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 for (int t = 0; t < 32; ++t) v[t] *= __ldg(gl0 + i0 + t);
                 umma::st32(tmem + lane_off + T_S + i0, v);
             }
-            if (c0 == c1) {
+            if (empty) {
                 uint16_t *cw = a.conv + ((size_t)dst * H + h) * (kConvW - 1) * CC;
                 for (int idx = tid; idx < (kConvW - 1) * CC; idx += 256)
                     cw[idx] = src >= 0 ? a.conv[((size_t)src * H + h) * (kConvW - 1) * CC + idx] : (uint16_t)0;
@@ -1218,18 +1238,20 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         bool ok = true;
         // checkpoint boundaries: a running next boundary, its slot fetched one boundary ahead (no division in
         // the loop); chunk entries are fetched one chunk ahead
-        const bool want_ck = a.interval > 0 && !(flag & kSeqCkptBad) && c0 < c1;
+        // (the boundaries at or before this launch's first position belong to the chunks before it)
+        const bool want_ck = a.interval > 0 && !(flag & kSeqCkptBad) && !empty;
         const int64_t send = start + ((int64_t)a.cu_seqlens[n + 1] - a.cu_seqlens[n]);
-        int64_t next_b = want_ck ? (start / a.interval + 1) * a.interval : INT64_MAX;
+        const int64_t pb = !empty ? pos[cb] : start;
+        int64_t next_b = want_ck ? (pb / a.interval + 1) * a.interval : INT64_MAX;
         const int32_t *cks = want_ck ? a.ckpt_slots + a.ckpt_offsets[n] : nullptr;
-        int jck = 0;
-        int ck_pre = (want_ck && next_b <= send) ? cks[0] : -1;
-        ChunkEnt e_nx = c0 < c1 ? ent[c0] : ChunkEnt{};
-        int64_t p_nx = c0 < c1 ? pos[c0] : 0;
-        for (int32_t c = c0; c < c1; ++c) {
+        int jck = want_ck ? (int)(pb / a.interval - start / a.interval) : 0;
+        int ck_pre = (want_ck && next_b <= send) ? cks[jck] : -1;
+        ChunkEnt e_nx = !empty ? ent[cb] : ChunkEnt{};
+        int64_t p_nx = pb;
+        for (int32_t c = cb; c < ce; ++c) {
             const ChunkEnt e = e_nx;
             const int64_t pend = p_nx + e.n;
-            const bool has_next = c + 1 < c1;
+            const bool has_next = c + 1 < ce;
             if (has_next) {
                 e_nx = ent[c + 1];
                 p_nx = pos[c + 1];
@@ -1331,10 +1353,13 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
 #pragma unroll
                         for (int t = 0; t < 32; ++t) v[t] *= gln[i0 + t];
                         umma::st32_issue(tmem + lane_off + T_S + i0, v);
-                    } else {
+                    } else if (last) {
 #pragma unroll
                         for (int t = 0; t < 32; ++t)
                             store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) carry[(size_t)(i0 + t) * D + j] = v[t];
                     }
                 };
                 s_part(ra, ia);
@@ -1342,7 +1367,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 umma::wait_st();
             }
             // ---- O^T -> the staging buffer of the output warps (once they have consumed the previous one) ----
-            if (c > c0) ok = __all_sync(0xffffffffu, mbar_wait(bar_empty, (uint32_t)(c - c0 - 1) & 1u) && ok);
+            if (c > cb) ok = __all_sync(0xffffffffu, mbar_wait(bar_empty, (uint32_t)(c - cb - 1) & 1u) && ok);
             ok = __all_sync(0xffffffffu, mbar_wait(bar_o, ph_o) && ok);
             ph_o ^= 1;
             umma::fence_after();
@@ -1376,10 +1401,10 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                             : make_uint2(0u, 0u);
             }
         };
-        if (c0 < c1) fetch_gates(c0);
-        for (int32_t c = c0; c < c1; ++c) {
+        if (!empty) fetch_gates(cb);
+        for (int32_t c = cb; c < ce; ++c) {
             const ChunkEnt e = ent[c];
-            if (!mbar_wait(bar_full, (uint32_t)(c - c0) & 1u)) {
+            if (!mbar_wait(bar_full, (uint32_t)(c - cb) & 1u)) {
                 if (lane == 0) set_status(a.status, KDA_DEV_TIMEOUT);
                 break;
             }
@@ -1420,7 +1445,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                                    (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
                 }
             }
-            if (c + 1 < c1) fetch_gates(c + 1);
+            if (c + 1 < ce) fetch_gates(c + 1);
         }
     }
     umma::fence_before();
@@ -1475,7 +1500,31 @@ static bool token_map(EncodeTiledFn enc, CUtensorMap *m, const void *base, int H
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
+// Segmented launches.  With few (sequence, head) chains the state kernel leaves most SMs idle while it walks
+// a long chunk chain after the intra kernel.  Such a call is cut into segments of kSegChunks chunks: the intra
+// kernel of segment s+1 runs on nsm - chains SMs while the state kernel of segment s runs on the other
+// `chains`, on a side stream that waits (events only, no device-side waiting) for the intra kernel of its
+// segment.  The state crosses a segment boundary in fp32 through the workspace and sees the same arithmetic
+// as at a chunk boundary inside one launch, so the results are identical to a single launch.
+constexpr int kSegChunks = 128;
+constexpr int64_t kSegMinChunks = 4 * kSegChunks;
+
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static SideStream *side_stream(int dev) {
+    static SideStream side[64];
+    if (dev < 0 || dev >= 64) return nullptr;
+    return &side[dev];
+}
+
+static int launch_prefill_tc(const PrefillArgs &a0, cudaStream_t st) {
+    PrefillArgs a = a0;
+    a.seg_lo = 0;
+    a.seg_hi = INT32_MAX;
     const tc::Layout2 L2 = tc::make_layout2(a.H, a.nseq, a.total_tokens);
     static int attr_done[64] = {0};
     int dev = 0;
@@ -1488,24 +1537,53 @@ static int launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
             return launch_result("prefill: cudaFuncSetAttribute");
         attr_done[dev] = 1;
     }
-    if (L2.maxc > 0x7fffffffLL || a.H > 65535) return fail(KDA_ERR_INVALID_ARG, "prefill: grid too large");
+    if (L2.maxc * a.H > 0x7fffffffLL || a.H > 65535) return fail(KDA_ERR_INVALID_ARG, "prefill: grid too large");
     prefill_table_kernel<<<1, kMaxSeqThreads, 0, st>>>(a, tc::as_layout(L2));
+    CUtensorMap tq, tk, tv, ta;
     if (a.total_tokens > 0) {
         const EncodeTiledFn enc = tensor_map_encoder();
         if (!enc) return fail(KDA_ERR_CUDA, "prefill: cuTensorMapEncodeTiled is not available");
-        CUtensorMap tq, tk, tv, ta;
         if (!token_map(enc, &tq, a.q, a.H, a.total_tokens, tc::RAW_ROWS) ||
             !token_map(enc, &tk, a.k, a.H, a.total_tokens, tc::RAW_ROWS) ||
             !token_map(enc, &tv, a.v, a.H, a.total_tokens, tc::RAW_ROWS) ||
             !token_map(enc, &ta, a.a, a.H, a.total_tokens, tc::CH))
             return fail(KDA_ERR_CUDA, "prefill: tensor map encoding failed");
-        const long long items = (long long)L2.maxc * a.H;  // an upper bound; the kernel reads the real count
-        const unsigned gi = (unsigned)std::min<long long>(items, current_device_sms());  // one CTA per SM
-        tc::prefill_intra_tc_kernel<<<gi, tc::NTI, tc::I_SMEM, st>>>(a, L2, tq, tk, tv, ta);
     }
-    dim3 gs(a.nseq, a.H);
-    tc::prefill_state_tc_kernel<<<gs, tc::NTS, tc::S_SMEM, st>>>(a, L2);
-    return launch_result("prefill (tensor-core path) launch");
+    const int nsm = current_device_sms();
+    const long long chains = (long long)a.nseq * a.H;
+    const dim3 gs(a.nseq, a.H);
+    if (a.total_tokens == 0 || chains * 4 > nsm || L2.maxc < kSegMinChunks) {
+        if (a.total_tokens > 0) {
+            const long long items = L2.maxc * a.H;  // an upper bound; the kernel reads the real count
+            const unsigned gi = (unsigned)std::min<long long>(items, nsm);  // one CTA per SM
+            tc::prefill_intra_tc_kernel<<<gi, tc::NTI, tc::I_SMEM, st>>>(a, L2, tq, tk, tv, ta);
+        }
+        tc::prefill_state_tc_kernel<<<gs, tc::NTS, tc::S_SMEM, st>>>(a, L2);
+        return launch_result("prefill (tensor-core path) launch");
+    }
+    SideStream *ss = side_stream(dev);
+    if (!ss) return fail(KDA_ERR_CUDA, "prefill: no side stream for this device");
+    std::lock_guard<std::mutex> lock(ss->mu);  // one segmented call at a time per device: the events are shared
+    if (!ss->stream) {
+        if (cudaStreamCreateWithFlags(&ss->stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss->join, cudaEventDisableTiming) != cudaSuccess)
+            return launch_result("prefill: side stream creation");
+    }
+    const unsigned gi = (unsigned)(nsm - chains);  // the intra CTAs leave one SM to each state CTA
+    bool forked = true;
+    for (long long lo = 0; lo < L2.maxc && forked; lo += kSegChunks) {
+        a.seg_lo = (int32_t)lo;
+        a.seg_hi = (int32_t)std::min<long long>(lo + kSegChunks, INT32_MAX);
+        tc::prefill_intra_tc_kernel<<<gi, tc::NTI, tc::I_SMEM, st>>>(a, L2, tq, tk, tv, ta);
+        forked = cudaEventRecord(ss->fork, st) == cudaSuccess && cudaStreamWaitEvent(ss->stream, ss->fork, 0) == cudaSuccess;
+        if (forked) tc::prefill_state_tc_kernel<<<gs, tc::NTS, tc::S_SMEM, ss->stream>>>(a, L2);
+    }
+    // the caller's stream always waits for the side stream, also after a failed fork
+    const bool joined =
+        cudaEventRecord(ss->join, ss->stream) == cudaSuccess && cudaStreamWaitEvent(st, ss->join, 0) == cudaSuccess;
+    if (!forked || !joined) return launch_result("prefill: segment fork / join");
+    return launch_result("prefill (tensor-core path, segmented) launch");
 }
 
 int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st) {

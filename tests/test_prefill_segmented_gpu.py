@@ -1,0 +1,172 @@
+"""Segmented prefill launches on the GPU (through the C ABI).
+
+A call whose (sequence, head) chains would leave most SMs idle in the chunk chain (chains x 4 <= SMs, at
+least 512 chunks) is launched in segments of 128 chunks: the intra kernel of one segment runs beside the
+state kernel of the segment before, and the state crosses a segment boundary in fp32 through the
+workspace.  The arithmetic at a segment boundary is that at a chunk boundary inside one launch, so every
+test here is bit-exact against the same work done by calls too small to be segmented:
+
+  * one sequence, resumed from a random state at an unaligned position (a partial first chunk), with a
+    checkpoint at every segment end, against the same tokens in two resumed calls;
+  * three sequences (one empty) whose chunks are cut by segments at arbitrary points, against one call
+    per sequence;
+  * a bf16 state pool against the fp32 pool rounded to bf16 (outputs identical, states and checkpoints
+    the bf16 rounding of the fp32 ones).
+
+The sizes are chosen so that the one-call side is segmented (at least 512 chunks, chains x 4 <= the SM
+count, asserted) and every call it is compared with is not (fewer than 512 chunks).  The oracle
+comparison of the segmented path at full size is the long-context test in test_prefill_gpu.py (one
+131072-token sequence, 32 heads).
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as ki
+from tests.kda_testutil import fill_pool
+
+pytestmark = pytest.mark.gpu
+
+D, CH = 128, 64
+
+
+def _kda():
+    import hybrid_linear_attention_decode_gb300 as kda
+    kda.load_library()
+    return kda
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _tokens(seed, T, H):
+    """bf16 token inputs drawn on the device (q, k, v, z ~ N(0,1), decay logits ~ N(3,1), beta logits ~ N(0,1))."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+
+    def draw(*shape, shift=0.0):
+        return (torch.randn(*shape, generator=g, device="cuda") + shift).to(torch.bfloat16)
+    return dict(q=draw(T, H, D), k=draw(T, H, D), v=draw(T, H, D), a=draw(T, H, D, shift=3.0), b=draw(T, H),
+                z=draw(T, H, D))
+
+
+def _ckpt_count(start, length, interval):
+    return (start + length) // interval - start // interval
+
+
+def _call(kda, pool, prm, tok, t0, lens, starts, src, dst, interval, ck_slots):
+    """One prefill call over tokens [t0, t0 + sum(lens)) of `tok`; returns y."""
+    T = int(sum(lens))
+    H = pool.S.shape[1]
+    i32 = lambda a: torch.tensor(np.asarray(a, dtype=np.int64), dtype=torch.int32, device="cuda")  # noqa: E731
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    counts = [_ckpt_count(s, l, interval) for s, l in zip(starts, lens)]
+    offs = np.concatenate([[0], np.cumsum(counts)])
+    assert len(ck_slots) == offs[-1]
+    sl = {k: v[t0:t0 + T].contiguous() for k, v in tok.items()}  # zero rows for an empty call
+    y = torch.empty(T, H, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(kda.kda_prefill_workspace_bytes(pool, len(lens), T, CH), 16), dtype=torch.uint8,
+                     device="cuda")
+    ws.fill_(0xCD)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_prefill_chunked(pool, prm, i32(cu), torch.tensor(starts, dtype=torch.int64, device="cuda"), i32(src),
+                            i32(dst), CH, interval, i32(offs), i32(ck_slots if len(ck_slots) else [0]), sl["q"],
+                            sl["k"], sl["v"], sl["a"], sl["b"], sl["z"], y, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return y
+
+
+def _setup(kda, H, num_slots, seed, sdt=torch.float32):
+    pool = kda.StatePool.empty(num_slots, H, D, D, state_dtype=sdt)
+    fill_pool(pool, seed)
+    wts = ki.layer_weights(seed, H, D, D)
+    prm = kda.LayerParams(torch.from_numpy(wts["conv_w"]).cuda(), torch.from_numpy(wts["norm_w"]).cuda())
+    return pool, prm
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32).cpu().numpy()
+
+
+def test_segmented_call_equals_two_resumed_calls():
+    kda = _kda()
+    # chunk 0 is [1064, 1088); the segment ends fall at 1024 + 8192 k, all multiples of the interval
+    H, interval, T, start = 32, 1024, 40000, 1064
+    assert H * 4 <= _sms() and T // CH >= 512
+    pool, prm = _setup(kda, H, 96, seed=81)
+    tok = _tokens(82, T, H)
+    cks = list(range(8, 8 + _ckpt_count(start, T, interval)))
+    assert len(cks) == 39
+    src_bits = _bits(pool.S[1])
+    # one call: the segmented path
+    yA = _call(kda, pool, prm, tok, 0, [T], [start], [1], [2], interval, cks)
+    SA, CA = _bits(pool.S[2]), _bits(pool.conv[2])
+    ckA = [(_bits(pool.S[s]), _bits(pool.conv[s])) for s in cks]
+    np.testing.assert_array_equal(_bits(pool.S[1]), src_bits)  # the source slot is untouched
+    # the same tokens in two calls small enough for single launches, resumed through slot 3 at a chunk-aligned
+    # position (a call boundary inside an aligned chunk would split that chunk differently)
+    T1 = 16024
+    assert (start + T1) % CH == 0
+    n1 = _ckpt_count(start, T1, interval)
+    cks_b = list(range(50, 50 + len(cks)))
+    y1 = _call(kda, pool, prm, tok, 0, [T1], [start], [1], [3], interval, cks_b[:n1])
+    y2 = _call(kda, pool, prm, tok, T1, [T - T1], [start + T1], [3], [4], interval, cks_b[n1:])
+    np.testing.assert_array_equal(_bits(yA), _bits(torch.cat([y1, y2])))
+    np.testing.assert_array_equal(SA, _bits(pool.S[4]))
+    np.testing.assert_array_equal(CA, _bits(pool.conv[4]))
+    for j, s in enumerate(cks_b):
+        np.testing.assert_array_equal(ckA[j][0], _bits(pool.S[s]), err_msg=f"checkpoint {j}")
+        np.testing.assert_array_equal(ckA[j][1], _bits(pool.conv[s]), err_msg=f"checkpoint window {j}")
+
+
+def test_segmented_call_equals_per_sequence_calls():
+    kda = _kda()
+    H, interval = 8, 4096
+    lens, starts, src, dst = [20000, 0, 15050], [0, 77, 3000], [-1, 5, 6], [1, 2, 3]
+    T = sum(lens)
+    assert len(lens) * H * 4 <= _sms() and T // CH >= 512
+    pool, prm = _setup(kda, H, 40, seed=91)
+    tok = _tokens(92, T, H)
+    counts = [_ckpt_count(s, l, interval) for s, l in zip(starts, lens)]
+    cks = list(range(8, 8 + sum(counts)))
+    yA = _call(kda, pool, prm, tok, 0, lens, starts, src, dst, interval, cks)
+    outA = [(_bits(pool.S[d]), _bits(pool.conv[d])) for d in dst]
+    ckA = [(_bits(pool.S[s]), _bits(pool.conv[s])) for s in cks]
+    # one call per sequence, each below the segmentation bound, into fresh slots
+    dstB = [21, 22, 23]
+    cksB = list(range(24, 24 + sum(counts)))
+    ys, t0, o = [], 0, 0
+    for n in range(len(lens)):
+        ys.append(_call(kda, pool, prm, tok, t0, [lens[n]], [starts[n]], [src[n]], [dstB[n]], interval,
+                        cksB[o:o + counts[n]]))
+        t0 += lens[n]
+        o += counts[n]
+    np.testing.assert_array_equal(_bits(yA), _bits(torch.cat(ys)))
+    for n, d in enumerate(dstB):
+        np.testing.assert_array_equal(outA[n][0], _bits(pool.S[d]), err_msg=f"state {n}")
+        np.testing.assert_array_equal(outA[n][1], _bits(pool.conv[d]), err_msg=f"window {n}")
+    for j, s in enumerate(cksB):
+        np.testing.assert_array_equal(ckA[j][0], _bits(pool.S[s]), err_msg=f"checkpoint {j}")
+        np.testing.assert_array_equal(ckA[j][1], _bits(pool.conv[s]), err_msg=f"checkpoint window {j}")
+
+
+def test_segmented_bf16_pool_is_the_rounded_fp32_pool():
+    kda = _kda()
+    H, interval, T = 32, 16384, 36000
+    assert H * 4 <= _sms() and T // CH >= 512
+    tok = _tokens(101, T, H)
+    cks = [4, 5]
+    res = {}
+    for sdt in (torch.float32, torch.bfloat16):
+        pool, prm = _setup(kda, H, 8, seed=102, sdt=sdt)
+        y = _call(kda, pool, prm, tok, 0, [T], [0], [-1], [1], interval, cks)
+        res[sdt] = (y, pool.S[1].clone(), [pool.S[s].clone() for s in cks], pool.conv[1].clone())
+    y32, S32, ck32, c32 = res[torch.float32]
+    y16, S16, ck16, c16 = res[torch.bfloat16]
+    np.testing.assert_array_equal(_bits(y32), _bits(y16))
+    np.testing.assert_array_equal(_bits(S32.to(torch.bfloat16)), _bits(S16))
+    for a, b in zip(ck32, ck16):
+        np.testing.assert_array_equal(_bits(a.to(torch.bfloat16)), _bits(b))
+    np.testing.assert_array_equal(_bits(c32), _bits(c16))
