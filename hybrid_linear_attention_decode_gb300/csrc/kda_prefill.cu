@@ -766,21 +766,20 @@ __global__ void __launch_bounds__(NTI, 1)
     const bool slow = __syncthreads_or(wide) != 0;
     uint8_t *X1 = sm + I_X1;
     uint8_t *Km = sm + I_KM;
-    for (int idx = tid; idx < CH * 16; idx += NTI) {
-        const int r = idx >> 4, i0 = (idx & 15) * 8;  // 8 channels per item, computed 4 at a time
-        uint32_t pk[4], pq[4], pm[4], pp[4];            // bf16 pairs of K+, Q+ (mid reference), K-, Q+ (chunk start)
-#pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {
-            const int ic = i0 + 4 * hq;
+    {   // one row per warp and four channels per thread: the 16-byte reads of G, k^ and q^ are consecutive
+        // across a warp, each 8-byte tile store fills a contiguous half-row, and G_mid / exp(G_mid) of the
+        // thread's channels are read once
+        const int ic = 4 * lane;
+        const float4 m4 = *reinterpret_cast<const float4 *>(G + MID * D + ic);
+        const float4 e4 = *reinterpret_cast<const float4 *>(eGm + ic);
+        const float gmv[4] = {m4.x, m4.y, m4.z, m4.w}, egv[4] = {e4.x, e4.y, e4.z, e4.w};
+        for (int r = warp; r < CH; r += NTI / 32) {
             const float4 g4 = *reinterpret_cast<const float4 *>(G + r * D + ic);
             const float4 k4 = *reinterpret_cast<const float4 *>(kh + r * D + ic);
             const float4 q4 = *reinterpret_cast<const float4 *>(qh + r * D + ic);
-            const float4 m4 = *reinterpret_cast<const float4 *>(G + MID * D + ic);
-            const float4 e4 = *reinterpret_cast<const float4 *>(eGm + ic);
             const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
-            const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, gmv[4] = {m4.x, m4.y, m4.z, m4.w};
-            const float egv[4] = {e4.x, e4.y, e4.z, e4.w};
-            float xk[4], xq[4], xm[4], xp[4];
+            const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+            float xk[4], xq[4], xm[4], xp[4];  // K+, Q+ (mid reference), K-, Q+ (chunk start)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float g = gv[u], k_ = kv[u], q_ = qv[u];
@@ -797,23 +796,17 @@ __global__ void __launch_bounds__(NTI, 1)
                 }
                 xp[u] = a.scale * q_ * eq;
             }
-            pk[2 * hq] = umma::pack_bf16(xk[0], xk[1]);
-            pk[2 * hq + 1] = umma::pack_bf16(xk[2], xk[3]);
-            pq[2 * hq] = umma::pack_bf16(xq[0], xq[1]);
-            pq[2 * hq + 1] = umma::pack_bf16(xq[2], xq[3]);
-            pm[2 * hq] = umma::pack_bf16(xm[0], xm[1]);
-            pm[2 * hq + 1] = umma::pack_bf16(xm[2], xm[3]);
-            pp[2 * hq] = umma::pack_bf16(xp[0], xp[1]);
-            pp[2 * hq + 1] = umma::pack_bf16(xp[2], xp[3]);
+            if (!slow) {
+                *reinterpret_cast<uint2 *>(X1 + umma::sw128_offset<2>(128, r, ic)) =
+                    make_uint2(umma::pack_bf16(xk[0], xk[1]), umma::pack_bf16(xk[2], xk[3]));
+                *reinterpret_cast<uint2 *>(X1 + umma::sw128_offset<2>(128, CH + r, ic)) =
+                    make_uint2(umma::pack_bf16(xq[0], xq[1]), umma::pack_bf16(xq[2], xq[3]));
+                *reinterpret_cast<uint2 *>(Km + umma::sw128_offset<2>(CH, r, ic)) =
+                    make_uint2(umma::pack_bf16(xm[0], xm[1]), umma::pack_bf16(xm[2], xm[3]));
+            }
+            *reinterpret_cast<uint2 *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, ic)) =
+                make_uint2(umma::pack_bf16(xp[0], xp[1]), umma::pack_bf16(xp[2], xp[3]));
         }
-        if (!slow) {
-            *reinterpret_cast<uint4 *>(X1 + umma::sw128_offset<2>(128, r, i0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4 *>(X1 + umma::sw128_offset<2>(128, CH + r, i0)) =
-                make_uint4(pq[0], pq[1], pq[2], pq[3]);
-            *reinterpret_cast<uint4 *>(Km + umma::sw128_offset<2>(CH, r, i0)) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
-        }
-        *reinterpret_cast<uint4 *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, i0)) =
-            make_uint4(pp[0], pp[1], pp[2], pp[3]);
     }
     fence_proxy_async_smem();
     umma::fence_before();
