@@ -589,11 +589,12 @@ def run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws):
 LONG_T, LONG_INTERVAL, LONG_DEC_N = 131072, 32768, 256
 
 
-def run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
+def run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws, prefill_only=False):
     """The long-context workload: one 131072-token prefill (H=32, d=128, chunk 64, checkpoints every 32768
     tokens) into the pool, then a batch-256 decode step in which request 0 continues that sequence from its
     final state and 255 requests use other random slots.  Token inputs are drawn on the device (seeded torch
-    generator, the distributions of the other workloads); 5 GB of them would be slow to draw on the host."""
+    generator, the distributions of the other workloads); 5 GB of them would be slow to draw on the host.
+    prefill_only: two prefill calls and nothing else (the profile case)."""
     T, C, I = LONG_T, PRE_CHUNK, LONG_INTERVAL
     ns = int(pool.S.shape[0])
     g = torch.Generator(device=dev)
@@ -620,7 +621,7 @@ def run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, w
     pre()
     torch.cuda.synchronize()
     barrier(ws)
-    Kp = 3
+    Kp = 1 if prefill_only else 3
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(Kp):
@@ -629,6 +630,8 @@ def run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, w
     torch.cuda.synchronize()
     pre_ms = max_over_ranks(e0.elapsed_time(e1), ws) / Kp
     del ws_buf, q, k, v, a, z, b, y
+    if prefill_only:
+        return {"prefill_ms": pre_ms, "status": int(status.item())}
     # decode at batch 256: request 0 continues the long sequence (in place), the rest use other slots
     N = LONG_DEC_N
     others = perm[1 + nck:1 + nck + N - 1]
@@ -726,7 +729,8 @@ def run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
 def run_profile_case(args):
     """Small case for ncu captures of one kernel: decode on a 768-slot pool (1.5 GiB fp32 or 0.8 GiB bf16
     states, larger than L2), batch 64, a fresh slot draw per launch; the 5-token verify step on the same
-    pool; or one prefill call of the benchmark's prefill workload."""
+    pool; one prefill call of the benchmark's prefill workload; or two calls of the long-context prefill
+    (one 131072-token sequence, launched in segments; for a launch list, not a multi-pass capture)."""
     import torch
     import hybrid_linear_attention_decode_gb300 as kda
     kda.load_library()
@@ -775,6 +779,11 @@ def run_profile_case(args):
     elif args.profile == "project":
         r = run_project(argparse.Namespace(steps=args.steps, warmup=args.warmup), kda, torch, dev, stream, seed, 1)
         print(f"profile case project: {r}")
+    elif args.profile == "long_prefill":
+        pool = kda.StatePool.empty(16, H, DK, DV, W, device=dev)
+        r = run_long_context(args, kda, torch, dev, stream, pool, prm, seed, 6666.0, 1, prefill_only=True)
+        assert r["status"] == 0
+        print(f"profile case long_prefill: {r}")
     else:
         pool = kda.StatePool.empty(512, H, DK, DV, W, device=dev)
         r = run_prefill(argparse.Namespace(steps=1, warmup=args.warmup), kda, torch, dev, stream, pool, prm, seed,
@@ -790,7 +799,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode_bf16", "decode_multi", "project", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_bf16", "decode_multi", "project", "prefill",
+                                              "long_prefill"], default=None,
                     help="run a small case of one kernel for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -700,8 +700,9 @@ __global__ void __launch_bounds__(NTI, 1)
         const int r3 = tid / (CC / 8), rem = tid - r3 * (CC / 8), part = rem >> 4, unit = rem & 15;
         wstash[tid] = reinterpret_cast<const uint4 *>(raw + part * RAW_PART + (ntok + r3) * D)[unit];
     }
-    {   // L2 norms: rows warp, warp + 16, warp + 32, warp + 48, their reductions interleaved
-        float sq[4], sk[4];
+    {   // L2 norms: rows warp, warp + 16, warp + 32, warp + 48, their reductions interleaved; the values stay
+        // in registers between the sums and the scaling
+        float sq[4], sk[4], vq[4][D / 32], vk[4][D / 32];
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
             const int r = warp + 16 * k4;
@@ -709,6 +710,8 @@ __global__ void __launch_bounds__(NTI, 1)
 #pragma unroll
             for (int i = 0; i < D / 32; ++i) {
                 const float xq = qh[r * D + lane + 32 * i], xk = kh[r * D + lane + 32 * i];
+                vq[k4][i] = xq;
+                vk[k4][i] = xk;
                 aq = fmaf(xq, xq, aq);
                 ak = fmaf(xk, xk, ak);
             }
@@ -729,8 +732,8 @@ __global__ void __launch_bounds__(NTI, 1)
             const float rq = rsqrtf(sq[k4] + a.l2_eps), rk = rsqrtf(sk[k4] + a.l2_eps);
 #pragma unroll
             for (int i = 0; i < D / 32; ++i) {
-                qh[r * D + lane + 32 * i] *= rq;
-                kh[r * D + lane + 32 * i] *= rk;
+                qh[r * D + lane + 32 * i] = vq[k4][i] * rq;
+                kh[r * D + lane + 32 * i] = vk[k4][i] * rk;
             }
         }
     }
