@@ -1168,6 +1168,10 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         bulk_g2s(ops + WS_KT, blk_of(c) + WS_KT, D * CH * 4 + D * 4, bar_b);  // Ktil^T and exp(G_last)
     };
 
+    // thread 0's record of the copies it issued and has not yet seen complete, with the parity of the phase
+    // that completes each (read only on the exit after a timed-out wait)
+    bool out_w = false, out_u = false, out_b = false;
+    uint32_t par_w = 0, par_u = 0, par_b = 0;
     if (warp == 0) umma::alloc(tmem_s, 256);
     for (int jj = tid; jj < D; jj += NTS) nw[jj] = __ldg(a.norm_w + jj);
     if (tid == 0) {
@@ -1181,6 +1185,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             issue_qp(cb);
             issue_u(cb);
             issue_b(cb);
+            out_w = out_u = out_b = true;
         }
     }
     umma::fence_before();
@@ -1264,6 +1269,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             // ---- U^T = S^T (-W)^T and O^T = S^T Q+^T (if -W / Q+ never arrive, nothing is committed and
             //      every thread's bounded wait on bar_mma gives up) ----
             if (tid == 0 && mbar_wait(bar_w, ph_w)) {
+                out_w = false;
                 const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
                 for (int ks = 0; ks < D / 16; ++ks)
                     umma::mma_bf16(tmem + T_U, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_W, CH, ks), idp, ks > 0);
@@ -1276,9 +1282,15 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             ok = mbar_wait(bar_mma, ph_m);
             ph_m ^= 1;
             umma::fence_after();
-            if (tid == 0 && ok && has_next) issue_w(c + 1);  // the U^T MMAs no longer read -W
+            if (tid == 0 && ok && has_next) {  // the U^T MMAs no longer read -W
+                issue_w(c + 1);
+                out_w = true;
+                par_w = ph_w;
+            }
             // ---- U = U' + U^T -> its tf32 and bf16 operand tiles ----
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_u, ph_u) && ok);  // warp-uniform: the load is a warp operation
+            const bool oku = mbar_wait(bar_u, ph_u);
+            if (oku) out_u = false;
+            ok = __all_sync(0xffffffffu, oku && ok);  // warp-uniform: the load is a warp operation
             ph_u ^= 1;
             if (ok) {
                 const float *up = reinterpret_cast<const float *>(ops + WS_UP);
@@ -1304,9 +1316,14 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             if (!ok) break;
             // ---- O^T += U^T Qk^T and S^T += U^T Ktil ----
             if (tid == 0) {
-                if (has_next) issue_u(c + 1);  // U' has been read by every thread
+                if (has_next) {  // U' has been read by every thread
+                    issue_u(c + 1);
+                    out_u = true;
+                    par_u = ph_u;
+                }
                 const bool okb = mbar_wait(bar_b, ph_b);
                 if (okb) {
+                    out_b = false;
                     const uint32_t ids = umma::idesc(umma::kTF32, 128, D);
                     for (int ks = 0; ks < CH / 8; ++ks)
                         umma::mma_tf32(tmem + T_S, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_KT, D, ks), ids,
@@ -1367,7 +1384,11 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             ok = __all_sync(0xffffffffu, mbar_wait(bar_o, ph_o) && ok);
             ph_o ^= 1;
             umma::fence_after();
-            if (tid == 0 && ok && has_next) issue_b(c + 1);  // every MMA of this chunk is done: Qk, Ktil^T free
+            if (tid == 0 && ok && has_next) {  // every MMA of this chunk is done: Qk, Ktil^T free
+                issue_b(c + 1);
+                out_b = true;
+                par_b = ph_b;
+            }
             if (ok) {
                 float v[32];
                 umma::ld32(tmem + lane_off + T_O + 32 * half, v);
@@ -1382,7 +1403,15 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             umma::fence_after();
             if (!ok) break;
         }
-        if (!ok && tid == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+        if (!ok && tid == 0) {
+            set_status(a.status, KDA_DEV_TIMEOUT);
+            // copies still in flight into this CTA's shared memory land before it exits (short bounded waits;
+            // the -W / Q+ phase never completes if Q+ was not issued, and that wait just runs out)
+            constexpr uint64_t kDrainNs = 10000000ull;
+            if (out_w) mbar_wait(bar_w, par_w, kDrainNs);
+            if (out_u) mbar_wait(bar_u, par_u, kDrainNs);
+            if (out_b) mbar_wait(bar_b, par_b, kDrainNs);
+        }
     } else {
         // ================================ output warps ================================
         const int ow = warp - 8;  // tokens ow, ow + 4, ..., one warp per token, 4 contiguous channels per lane

@@ -187,6 +187,12 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_pool *pool, int32_t nseq, i
  *   workspace   device, at least kda_prefill_workspace_bytes() bytes, contents need not be initialised
  * Same aliasing rules as decode, with checkpoint slots counting as dst slots.
  * Supported: (dk, dv) as for decode, W = 4, chunk in {16, 64}.
+ * Streams: all work is ordered on `stream`.  At dk = dv = 128, chunk 64, a call with few
+ * (sequence, head) chains (nseq*H*4 <= SM count) and at least 512 chunks is launched in segments.
+ * The chunk chain of each segment then runs on a library-owned side stream, beside the next segment's
+ * intra-chunk kernel.  The side stream forks from `stream` and joins it again before the call returns
+ * (events only), so this works under CUDA graph capture too.  Segmented calls on one device are
+ * serialised by a host lock.  The results are bit-identical to one launch.
  */
 KDA_API int kda_prefill_chunked(const kda_pool *pool, const kda_params *prm, int32_t nseq, int64_t total_tokens,
                         const int32_t *cu_seqlens, const int64_t *start_pos, const int32_t *src_slot,

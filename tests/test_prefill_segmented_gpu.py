@@ -12,7 +12,8 @@ test here is bit-exact against the same work done by calls too small to be segme
   * three sequences (one empty) whose chunks are cut by segments at arbitrary points, against one call
     per sequence;
   * a bf16 state pool against the fp32 pool rounded to bf16 (outputs identical, states and checkpoints
-    the bf16 rounding of the fp32 ones).
+    the bf16 rounding of the fp32 ones);
+  * a call captured in a CUDA graph and replayed, against the eager call.
 
 The sizes are chosen so that the one-call side is segmented (at least 512 chunks, chains x 4 <= the SM
 count, asserted) and every call it is compared with is not (fewer than 512 chunks).  The oracle
@@ -175,3 +176,33 @@ def test_segmented_bf16_pool_is_the_rounded_fp32_pool():
     for a, b in zip(ck32, ck16):
         np.testing.assert_array_equal(_bits(a.to(torch.bfloat16)), _bits(b))
     np.testing.assert_array_equal(_bits(c32), _bits(c16))
+
+
+def test_segmented_call_under_graph_capture():
+    """The side stream forks from the capturing stream and joins it again, so a segmented call captured in a
+    CUDA graph replays to the same bits as the eager call."""
+    kda = _kda()
+    H, interval, T = 32, 8192, 36000
+    assert H * 4 <= _sms() and T // CH >= 512
+    pool, prm = _setup(kda, H, 16, seed=111)
+    tok = _tokens(112, T, H)
+    cks_e, cks_g = [2, 3, 4, 5], [7, 8, 9, 10]
+    y_e = _call(kda, pool, prm, tok, 0, [T], [0], [-1], [1], interval, cks_e)  # eager; also the warm-up
+    i32 = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")  # noqa: E731
+    cu, sp, src, dst = i32([0, T]), torch.zeros(1, dtype=torch.int64, device="cuda"), i32([-1]), i32([6])
+    offs, cks = i32([0, len(cks_g)]), i32(cks_g)
+    y_g = torch.empty(T, H, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(pool, 1, T, CH), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kda.kda_prefill_chunked(pool, prm, cu, sp, src, dst, CH, interval, offs, cks, tok["q"], tok["k"], tok["v"],
+                                tok["a"], tok["b"], tok["z"], y_g, ws, st)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert _same(y_g, y_e)
+    assert _same(pool.S[6], pool.S[1]) and _same(pool.conv[6], pool.conv[1])
+    for a, b in zip(cks_e, cks_g):
+        assert _same(pool.S[a], pool.S[b]) and _same(pool.conv[a], pool.conv[b])
