@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kThreads) prefill_out_kernel(const PrefillArgs
 
 // ================================================================================ tensor-core path
 // dk = dv = 128, chunk 64.  Transposed formulation so that every MMA has M = 128 (TMEM lane = row):
-//   [A ; Qk]  = [K+ ; Q+] (mid-chunk reference) x K-^T           bf16, M=128 N=64  K=128
+//   [A ; Qk]  = [K+ ; Q+] (mid-chunk reference) x K-^T           tf32, M=128 N=64  K=128 (two halves)
 //   W^T       = (k*exp(G))^T x T^T,   U'^T = V^T x T^T            tf32, M=128 N=64  K=64
 //   U^T       = U'^T + S^T x (-W)^T                                bf16, M=128 N=64  K=128
 //   O^T       = S^T x Q+^T + U^T x Qk^T                            bf16, M=128 N=64  K=128 / 64
@@ -518,7 +518,7 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 // Intra-chunk kernel smem (bytes, from a 1024-aligned base), by phase:
 //   P0-P1  [0,32K) q^ fp32 | [32K,64K) k^ fp32 | [64K,96K) G fp32 (decay logits staged in its first 16K) |
 //          [96K,128K) V^T tf32 tile | [128K,180K) raw rows
-//   P2     [128K,160K) [K+;Q+] bf16 tile | [160K,176K) K- bf16 tile
+//   P2     [128K,160K) [K+;Q+] tf32 tile | [160K,176K) K- tf32 tile (one channel half at a time)
 //   P3-P4  [0,8K) Qk staging, then [0,17K) Inv fp32 (row stride 68) | [128K,145K) A fp32 (row stride 68) | [160K,176K) block temps,
 //          then T tf32
 //   P5     [0,32K) (k exp G)^T tf32 tile | [128K,160K) Ktil^T tf32 staging
@@ -767,64 +767,91 @@ __global__ void __launch_bounds__(NTI, 1)
         reinterpret_cast<float *>(blk + WS_GL)[tid] = expf(gl);
     }
     const bool slow = __syncthreads_or(wide) != 0;
-    uint8_t *X1 = sm + I_X1;
-    uint8_t *Km = sm + I_KM;
-    {   // one row per warp and four channels per thread: the 16-byte reads of G, k^ and q^ are consecutive
-        // across a warp, each 8-byte tile store fills a contiguous half-row, and G_mid / exp(G_mid) of the
-        // thread's channels are read once
-        const int ic = 4 * lane;
-        const float4 m4 = *reinterpret_cast<const float4 *>(G + MID * D + ic);
-        const float4 e4 = *reinterpret_cast<const float4 *>(eGm + ic);
-        const float gmv[4] = {m4.x, m4.y, m4.z, m4.w}, egv[4] = {e4.x, e4.y, e4.z, e4.w};
-        for (int r = warp; r < CH; r += NTI / 32) {
-            const float4 g4 = *reinterpret_cast<const float4 *>(G + r * D + ic);
-            const float4 k4 = *reinterpret_cast<const float4 *>(kh + r * D + ic);
-            const float4 q4 = *reinterpret_cast<const float4 *>(qh + r * D + ic);
-            const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
-            const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-            float xk[4], xq[4], xm[4], xp[4];  // K+, Q+ (mid reference), K-, Q+ (chunk start)
+    uint8_t *X1 = sm + I_X1;  // [K+; Q+] tf32 [128 rows][64 channels] of one channel half
+    uint8_t *Km = sm + I_KM;  // K- tf32 [64 rows][64 channels] of one channel half
+    {   // The [A; Qk] MMA takes tf32 operands and runs in two channel halves whose tiles take the space of one
+        // bf16 tile over all channels.  The operands of half 1 are formed in registers while the MMAs of half
+        // 0 run, and stored once those MMAs have read the tiles.  Rows warp + 16 j, two channels per thread
+        // per half: the 8-byte reads of G, k^ and q^ are consecutive across a warp and each 8-byte tile store
+        // fills a contiguous row chunk.
+        const int c2 = 2 * lane;
+        float xk[4][2], xq[4][2], xm[4][2];  // K+, Q+ (mid reference), K- of the thread's rows and channels
+        auto form = [&](int hh) {  // ... of channel half hh; Q+ (chunk start) of that half to the workspace
+            const int ic = 64 * hh + c2;
+            const float2 m2 = *reinterpret_cast<const float2 *>(G + MID * D + ic);
+            const float2 e2 = *reinterpret_cast<const float2 *>(eGm + ic);
+            const float gmv[2] = {m2.x, m2.y}, egv[2] = {e2.x, e2.y};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float g = gv[u], k_ = kv[u], q_ = qv[u];
-                float eq;
-                if (!slow) {
-                    const float ep = __expf(g - gmv[u]);
-                    xk[u] = k_ * ep;
-                    xq[u] = q_ * ep;
-                    xm[u] = k_ * __expf(gmv[u] - g);
-                    eq = ep * egv[u];
-                } else {
-                    xk[u] = xq[u] = xm[u] = 0.f;
-                    eq = __expf(g);
+            for (int j = 0; j < 4; ++j) {
+                const int r = warp + 16 * j;
+                const float2 g2 = *reinterpret_cast<const float2 *>(G + r * D + ic);
+                const float2 k2 = *reinterpret_cast<const float2 *>(kh + r * D + ic);
+                const float2 q2 = *reinterpret_cast<const float2 *>(qh + r * D + ic);
+                const float gv[2] = {g2.x, g2.y}, kv[2] = {k2.x, k2.y}, qv[2] = {q2.x, q2.y};
+                float xp[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const float g = gv[u], k_ = kv[u], q_ = qv[u];
+                    float eq;
+                    if (!slow) {
+                        const float ep = __expf(g - gmv[u]);
+                        xk[j][u] = k_ * ep;
+                        xq[j][u] = q_ * ep;
+                        xm[j][u] = k_ * __expf(gmv[u] - g);
+                        eq = ep * egv[u];
+                    } else {
+                        xk[j][u] = xq[j][u] = xm[j][u] = 0.f;
+                        eq = __expf(g);
+                    }
+                    xp[u] = a.scale * q_ * eq;
                 }
-                xp[u] = a.scale * q_ * eq;
+                *reinterpret_cast<uint32_t *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, ic)) =
+                    umma::pack_bf16(xp[0], xp[1]);
             }
-            if (!slow) {
-                *reinterpret_cast<uint2 *>(X1 + umma::sw128_offset<2>(128, r, ic)) =
-                    make_uint2(umma::pack_bf16(xk[0], xk[1]), umma::pack_bf16(xk[2], xk[3]));
-                *reinterpret_cast<uint2 *>(X1 + umma::sw128_offset<2>(128, CH + r, ic)) =
-                    make_uint2(umma::pack_bf16(xq[0], xq[1]), umma::pack_bf16(xq[2], xq[3]));
-                *reinterpret_cast<uint2 *>(Km + umma::sw128_offset<2>(CH, r, ic)) =
-                    make_uint2(umma::pack_bf16(xm[0], xm[1]), umma::pack_bf16(xm[2], xm[3]));
+        };
+        auto store = [&]() {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = warp + 16 * j;
+                *reinterpret_cast<uint2 *>(X1 + umma::sw128_offset<4>(128, r, c2)) =
+                    make_uint2(umma::to_tf32(xk[j][0]), umma::to_tf32(xk[j][1]));
+                *reinterpret_cast<uint2 *>(X1 + umma::sw128_offset<4>(128, CH + r, c2)) =
+                    make_uint2(umma::to_tf32(xq[j][0]), umma::to_tf32(xq[j][1]));
+                *reinterpret_cast<uint2 *>(Km + umma::sw128_offset<4>(CH, r, c2)) =
+                    make_uint2(umma::to_tf32(xm[j][0]), umma::to_tf32(xm[j][1]));
             }
-            *reinterpret_cast<uint2 *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, ic)) =
-                make_uint2(umma::pack_bf16(xp[0], xp[1]), umma::pack_bf16(xp[2], xp[3]));
+        };
+        auto mma = [&](int hh) {  // [A; Qk] (+)= [K+; Q+] K-^T over the 64 channels of half hh
+            fence_proxy_async_smem();
+            umma::fence_before();
+            __syncthreads();
+            umma::fence_after();
+            if (tid == 0) {
+                const uint32_t id = umma::idesc(umma::kTF32, 128, CH);
+                for (int ks = 0; ks < 64 / 8; ++ks)
+                    umma::mma_tf32(tmem, umma::sdesc_k(X1, 128, ks), umma::sdesc_k(Km, CH, ks), id, hh > 0 || ks > 0);
+                umma::commit(bar);
+            }
+        };
+        form(0);
+        if (!slow) {
+            store();
+            mma(0);
+            form(1);
+            ok = wait_all(bar, phase);  // the half-0 MMAs have read the tiles
+            phase ^= 1;
+            umma::fence_after();
+            if (ok) {
+                store();
+                mma(1);
+                ok = wait_all(bar, phase);
+                phase ^= 1;
+                umma::fence_after();
+            }
+        } else {
+            form(1);
+            __syncthreads();
         }
-    }
-    fence_proxy_async_smem();
-    umma::fence_before();
-    __syncthreads();
-    umma::fence_after();
-    if (!slow) {
-        if (tid == 0) {
-            const uint32_t id = umma::idesc(umma::kBF16, 128, CH);
-            for (int ks = 0; ks < D / 16; ++ks)
-                umma::mma_bf16(tmem, umma::sdesc_k(X1, 128, ks), umma::sdesc_k(Km, CH, ks), id, ks > 0);
-            umma::commit(bar);
-        }
-        ok = wait_all(bar, phase);
-        phase ^= 1;
-        umma::fence_after();
     }
     // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with diagonal, bf16 tile) ----
     float *A = reinterpret_cast<float *>(sm + I_A);      // [64][AST]
