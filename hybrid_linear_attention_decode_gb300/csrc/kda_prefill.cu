@@ -12,14 +12,21 @@
 // Chunks are aligned to absolute token positions (start_pos + i), so a sequence resumed at a chunk
 // boundary performs exactly the arithmetic of a full replay from that boundary on.
 //
-// Launches (one stream, graph-capturable):
-//   1. table:  validates cu_seqlens / start_pos / checkpoint offsets, builds the chunk table;
-//   2. intra:  one CTA per (chunk, head): causal conv + SiLU, L2 norms, gates, A, Qk, the unit-lower
-//              triangular solve, W / U' / decayed K / decayed Q into the workspace; conv windows of
-//              checkpoints and of the final state go straight to the pool;
-//   3. state:  one CTA per (sequence, head, dv tile), sequential over the sequence's chunks: U, O and the
-//              state chain in fp32; checkpoint states written at every boundary, the final one to dst;
-//   4. out:    gated RMSNorm of O into the bf16 output.
+// Two implementations, both graph-capturable:
+//   * SIMT fp32, for every supported shape (chunk 16 or 64), four launches on the caller's stream:
+//     1. table:  validates cu_seqlens / start_pos / checkpoint offsets, builds the chunk table;
+//     2. intra:  one CTA per (chunk, head): causal conv + SiLU, L2 norms, gates, A, Qk, the unit-lower
+//                triangular solve, W / U' / decayed K / decayed Q into the workspace; conv windows of
+//                checkpoints and of the final state go straight to the pool;
+//     3. state:  one CTA per (sequence, head, dv tile), sequential over the sequence's chunks: U, O and
+//                the state chain in fp32; checkpoint states at every boundary, the final one to dst;
+//     4. out:    gated RMSNorm of O into the bf16 output.
+//   * tcgen05 (namespace tc), for dk = dv = 128 and chunk 64: the same table, then a persistent intra
+//     kernel (one CTA per SM looping over (chunk, head) items, operand tiles written to the workspace in
+//     their shared-memory layout) and a state kernel (one CTA per (sequence, head): the chunk chain with
+//     S^T in tensor memory, the gated RMSNorm on separate warps beside it).  A long call with few
+//     (sequence, head) chains is launched in segments, the state chain of one segment running on a side
+//     stream beside the intra kernel of the next (launch_prefill_tc).
 #include <cuda.h>  // CUtensorMap; the encoder is looked up at run time, so nothing links the driver library
 
 #include <algorithm>
