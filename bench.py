@@ -781,13 +781,14 @@ def run_profile_case(args):
         print(f"profile case project: {r}")
     elif args.profile == "long_prefill":
         pool = kda.StatePool.empty(16, H, DK, DV, W, device=dev)
-        r = run_long_context(args, kda, torch, dev, stream, pool, prm, seed, 6666.0, 1, prefill_only=True)
+        r = run_long_context(args, kda, torch, dev, stream, pool, prm, seed, measured_peaks()[0], 1,
+                             prefill_only=True)
         assert r["status"] == 0
         print(f"profile case long_prefill: {r}")
     else:
         pool = kda.StatePool.empty(512, H, DK, DV, W, device=dev)
         r = run_prefill(argparse.Namespace(steps=1, warmup=args.warmup), kda, torch, dev, stream, pool, prm, seed,
-                        6666.0, 1)
+                        measured_peaks()[0], 1)
         print(f"profile case prefill: {r}")
 
 
