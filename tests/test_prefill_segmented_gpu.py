@@ -13,7 +13,9 @@ test here is bit-exact against the same work done by calls too small to be segme
     per sequence;
   * a bf16 state pool against the fp32 pool rounded to bf16 (outputs identical, states and checkpoints
     the bf16 rounding of the fp32 ones);
-  * a call captured in a CUDA graph and replayed, against the eager call.
+  * a call captured in a CUDA graph and replayed, against the eager call;
+and, against the fp64 oracle, one head (so that a segmented workspace fits the no-alloc entry point's
+static scratch) with a bf16 pool resumed from a stored state, no output gate and a skipped checkpoint.
 
 The sizes are chosen so that the one-call side is segmented (at least 512 chunks, chains x 4 <= the SM
 count, asserted) and every call it is compared with is not (fewer than 512 chunks).  The oracle
@@ -25,7 +27,7 @@ import pytest
 import torch
 
 import kda_inputs as ki
-from tests.kda_testutil import fill_pool
+from tests.kda_testutil import fill_pool, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -206,3 +208,28 @@ def test_segmented_call_under_graph_capture():
     assert _same(pool.S[6], pool.S[1]) and _same(pool.conv[6], pool.conv[1])
     for a, b in zip(cks_e, cks_g):
         assert _same(pool.S[a], pool.S[b]) and _same(pool.conv[a], pool.conv[b])
+
+
+def test_segmented_single_head_bf16_resume_noalloc_against_oracle():
+    """33 000 tokens of one head: 518 chunks, so the call is segmented, and a workspace of about 55 MB, within
+    the no-alloc scratch.  bf16 pool, resumed from a stored state at position 77 (a partial first chunk), no
+    output gate, checkpoints every 4096 tokens with one skipped; outputs, final state, every checkpoint and
+    every conv window against the fp64 oracle."""
+    from tests.test_prefill_gpu import Problem
+    kda = _kda()
+    H, T = 1, 33000
+    assert H * 4 <= _sms() and T // CH >= 512
+    p = Problem(kda, H, D, D, [T], [77], [3], [5], CH, 4096, 24, seed=121, with_z=False, ckpt_skip=(2,), sbf16=True)
+    assert kda.kda_prefill_workspace_bytes(p.pool, 1, T, CH) <= kda.NOALLOC_SCRATCH_BYTES
+    d = {k: (to_dev_bf16(v) if v is not None else None) for k, v in p.tok.items()}
+    p.y = torch.empty(T, H, D, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t = lambda a, dt: torch.tensor(np.asarray(a), dtype=dt, device="cuda")  # noqa: E731
+    kda.kda_prefill_chunked_noalloc(p.pool, p.prm, t(p.cu, torch.int32), t(p.starts, torch.int64),
+                                    t(p.src, torch.int32), t(p.dst, torch.int32), CH, p.interval,
+                                    t(p.offs, torch.int32), t(p.ck, torch.int32), d["q"], d["k"], d["v"], d["a"],
+                                    d["b"], d["z"], p.y, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert len(p.ck) == 8 and p.ck[2] == -1
+    p.check(p.reference())
