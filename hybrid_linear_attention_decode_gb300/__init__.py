@@ -304,9 +304,12 @@ def kda_prefill_chunked_noalloc(pool: StatePool, params: LayerParams, cu_seqlens
                                 dev_status, stream=None) -> None:
     """kda_prefill_chunked for callers that cannot allocate device memory: the workspace is the library's
     fixed scratch (NOALLOC_SCRATCH_BYTES per GPU).  Calls that overlap on the GPU race on that scratch;
-    the first call on a device should precede any stream capture.  See include/kda.h."""
+    the first call on a device (nseq = 0 does only that set-up) should come at start-up, before any stream
+    capture.  See include/kda.h."""
     nseq = int(start_pos.shape[0])
     T = int(q.shape[0]) if q is not None else 0
+    if _DEBUG_SLOTS and nseq > 0:
+        kda_check_slots(pool.num_slots, src_slot, dst_slot, ckpt_slots if ckpt_interval > 0 else None)
     pc, pp = pool.c(), params.c()
     rc = load_library().kda_prefill_chunked_noalloc(
         ctypes.byref(pc), ctypes.byref(pp), nseq, T, _ptr(cu_seqlens), _ptr(start_pos), _ptr(src_slot),

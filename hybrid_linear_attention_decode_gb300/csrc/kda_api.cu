@@ -66,6 +66,39 @@ static int check_pool(const kda_pool *pool, const kda_params *prm) {
     return KDA_OK;
 }
 
+int check_prefill_args(const kda_pool *pool, const kda_params *prm, int32_t nseq, int64_t total_tokens,
+                       const int32_t *cu_seqlens, const int64_t *start_pos, const int32_t *src_slot,
+                       const int32_t *dst_slot, int32_t chunk, int64_t ckpt_interval, const int32_t *ckpt_offsets,
+                       const int32_t *ckpt_slots, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const uint16_t *a, const uint16_t *b, const uint16_t *z, const uint16_t *y,
+                       const int32_t *dev_status) {
+    int rc = check_pool(pool, prm);
+    if (rc != KDA_OK) return rc;
+    if (!prm) return fail(KDA_ERR_INVALID_ARG, "prefill: params is NULL");
+    if (nseq < 0 || total_tokens < 0 || ckpt_interval < 0)
+        return fail(KDA_ERR_INVALID_ARG, "prefill: nseq, total_tokens and ckpt_interval must be >= 0");
+    if (!prefill_supported(pool->dk, pool->dv, pool->conv_w, chunk))
+        return fail(KDA_ERR_UNSUPPORTED_SHAPE, "prefill: (dk, dv, conv_w, chunk) not compiled in");
+    if (ckpt_interval > 0 && ckpt_interval % chunk != 0)
+        return fail(KDA_ERR_INVALID_ARG, "prefill: ckpt_interval is not a multiple of the chunk");
+    if (nseq == 0) return KDA_OK;
+    if (!cu_seqlens || !start_pos || !src_slot || !dst_slot)
+        return fail(KDA_ERR_INVALID_ARG, "prefill: cu_seqlens, start_pos, src_slot or dst_slot is NULL");
+    if (ckpt_interval > 0 && (!ckpt_offsets || !ckpt_slots))
+        return fail(KDA_ERR_INVALID_ARG, "prefill: checkpoints requested without ckpt_offsets / ckpt_slots");
+    if (total_tokens > 0 && (!q || !k || !v || !a || !b || !y))
+        return fail(KDA_ERR_INVALID_ARG, "prefill: a token tensor is NULL");
+    if (total_tokens * (int64_t)pool->H > ((int64_t)1 << 40))
+        return fail(KDA_ERR_INVALID_ARG, "prefill: total_tokens * H too large");
+    if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) || (a && !aligned16(a)) ||
+        (z && !aligned16(z)) || (y && !aligned16(y)))
+        return fail(KDA_ERR_INVALID_ARG, "prefill: q, k, v, a, z and y must be 16-byte aligned");
+    if ((b && !aligned2(b)) || !aligned4(cu_seqlens) || (reinterpret_cast<uintptr_t>(start_pos) & 7u) ||
+        !aligned4(src_slot) || !aligned4(dst_slot) || (dev_status && !aligned4(dev_status)))
+        return fail(KDA_ERR_INVALID_ARG, "prefill: b, tables, slot arrays or status misaligned");
+    return KDA_OK;
+}
+
 }  // namespace kda
 
 using namespace kda;
@@ -262,30 +295,9 @@ int kda_prefill_chunked(const kda_pool *pool, const kda_params *prm, int32_t nse
                         const uint16_t *a, const uint16_t *b, const uint16_t *z, uint16_t *y, void *workspace,
                         size_t workspace_bytes, int32_t *dev_status, kda_stream_t stream) {
     clear_error();
-    int rc = check_pool(pool, prm);
-    if (rc != KDA_OK) return rc;
-    if (!prm) return fail(KDA_ERR_INVALID_ARG, "prefill: params is NULL");
-    if (nseq < 0 || total_tokens < 0 || ckpt_interval < 0)
-        return fail(KDA_ERR_INVALID_ARG, "prefill: nseq, total_tokens and ckpt_interval must be >= 0");
-    if (!prefill_supported(pool->dk, pool->dv, pool->conv_w, chunk))
-        return fail(KDA_ERR_UNSUPPORTED_SHAPE, "prefill: (dk, dv, conv_w, chunk) not compiled in");
-    if (ckpt_interval > 0 && ckpt_interval % chunk != 0)
-        return fail(KDA_ERR_INVALID_ARG, "prefill: ckpt_interval is not a multiple of the chunk");
-    if (nseq == 0) return KDA_OK;
-    if (!cu_seqlens || !start_pos || !src_slot || !dst_slot)
-        return fail(KDA_ERR_INVALID_ARG, "prefill: cu_seqlens, start_pos, src_slot or dst_slot is NULL");
-    if (ckpt_interval > 0 && (!ckpt_offsets || !ckpt_slots))
-        return fail(KDA_ERR_INVALID_ARG, "prefill: checkpoints requested without ckpt_offsets / ckpt_slots");
-    if (total_tokens > 0 && (!q || !k || !v || !a || !b || !y))
-        return fail(KDA_ERR_INVALID_ARG, "prefill: a token tensor is NULL");
-    if (total_tokens * (int64_t)pool->H > ((int64_t)1 << 40))
-        return fail(KDA_ERR_INVALID_ARG, "prefill: total_tokens * H too large");
-    if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) || (a && !aligned16(a)) ||
-        (z && !aligned16(z)) || (y && !aligned16(y)))
-        return fail(KDA_ERR_INVALID_ARG, "prefill: q, k, v, a, z and y must be 16-byte aligned");
-    if ((b && !aligned2(b)) || !aligned4(cu_seqlens) || (reinterpret_cast<uintptr_t>(start_pos) & 7u) ||
-        !aligned4(src_slot) || !aligned4(dst_slot) || (dev_status && !aligned4(dev_status)))
-        return fail(KDA_ERR_INVALID_ARG, "prefill: b, tables, slot arrays or status misaligned");
+    const int rc = check_prefill_args(pool, prm, nseq, total_tokens, cu_seqlens, start_pos, src_slot, dst_slot, chunk,
+                                      ckpt_interval, ckpt_offsets, ckpt_slots, q, k, v, a, b, z, y, dev_status);
+    if (rc != KDA_OK || nseq == 0) return rc;
     const size_t need = prefill_workspace_bytes(pool->H, pool->dk, pool->dv, nseq, total_tokens, chunk);
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
         return fail(KDA_ERR_WORKSPACE, "prefill: workspace NULL, misaligned or smaller than "

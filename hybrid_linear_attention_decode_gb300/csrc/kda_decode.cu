@@ -138,6 +138,19 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF, SBF>::NT, DecodeShap
     if (tid == 0)
         for (int b = 0; b < NBUF; ++b) issue(b, blockIdx.x + b * gridDim.x);
 
+    // Thread 0, on the exit after a timed-out wait in iteration `it`: copies issued for iterations it ..
+    // it + NBUF - 1 (one per buffer, the last phase armed on its barriers) may still be landing in this CTA's
+    // shared memory; wait for each, briefly and bounded, before the CTA exits.
+    auto drain = [&](int it) {
+        constexpr uint64_t kDrainNs = 10000000ull;
+        for (int j = it; j < it + NBUF && blockIdx.x + j * (int)gridDim.x < nitems; ++j) {
+            const int b = j % NBUF;
+            const uint32_t p = (uint32_t)(j / NBUF) & 1u;
+            mbar_wait(&bar_in[b], p, kDrainNs);
+            for (int s = 0; s < NST; ++s) mbar_wait(&bar_S[b * NST + s], p, kDrainNs);
+        }
+    };
+
     const int g = tid / LPR, cg = tid - (tid / LPR) * LPR;
     for (int it = 0;; ++it) {
         const int item = blockIdx.x + it * gridDim.x;
@@ -166,7 +179,10 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF, SBF>::NT, DecodeShap
 
         bool fail = !mbar_wait(&bar_in[buf], par);
         if (__syncthreads_or(fail)) {
-            if (tid == 0) set_status(args.status, KDA_DEV_TIMEOUT);
+            if (tid == 0) {
+                set_status(args.status, KDA_DEV_TIMEOUT);
+                drain(it);
+            }
             return;
         }
         if (!ok) {
@@ -262,7 +278,10 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV, NBUF, SBF>::NT, DecodeShap
         *reinterpret_cast<float4 *>(red_k + g * DV + cg * 4) = accK;
         *reinterpret_cast<float4 *>(red_q + g * DV + cg * 4) = accQ;
         if (__syncthreads_or(sfail)) {
-            if (tid == 0) set_status(args.status, KDA_DEV_TIMEOUT);
+            if (tid == 0) {
+                set_status(args.status, KDA_DEV_TIMEOUT);
+                drain(it);
+            }
             return;
         }
         // the buffer is no longer read: start the copies of a later item into it

@@ -136,6 +136,15 @@ __global__ void __launch_bounds__(MultiShape<DK, DV, SBF>::NT, MultiShape<DK, DV
 
     if (tid == 0) issue(0, blockIdx.x);
 
+    // Thread 0, on the exit after a timed-out wait in an item: that item's copies (the next item's are issued
+    // only after its state has been read) may still be landing in this CTA's shared memory; wait for them,
+    // briefly and bounded, before the CTA exits.
+    auto drain = [&](int ib, uint32_t par_in, uint32_t par_S) {
+        constexpr uint64_t kDrainNs = 10000000ull;
+        mbar_wait(&bar_in[ib], par_in, kDrainNs);
+        for (int s = 0; s < NST; ++s) mbar_wait(&bar_S[s], par_S, kDrainNs);
+    };
+
     const int g = tid / LPR, cg = tid - (tid / LPR) * LPR;
     for (int it = 0;; ++it) {
         const int item = blockIdx.x + it * gridDim.x;
@@ -155,7 +164,10 @@ __global__ void __launch_bounds__(MultiShape<DK, DV, SBF>::NT, MultiShape<DK, DV
         }
         const bool fail = !mbar_wait(&bar_in[ib], par_in);
         if (__syncthreads_or(fail)) {
-            if (tid == 0) set_status(args.status, KDA_DEV_TIMEOUT);
+            if (tid == 0) {
+                set_status(args.status, KDA_DEV_TIMEOUT);
+                drain(ib, par_in, par_S);
+            }
             return;
         }
         if (!request_ok(n)) {
@@ -269,7 +281,10 @@ __global__ void __launch_bounds__(MultiShape<DK, DV, SBF>::NT, MultiShape<DK, DV
             *reinterpret_cast<float4 *>(red_k + g * DV + cg * 4) = accK;
             *reinterpret_cast<float4 *>(red_q + g * DV + cg * 4) = accQ;
             if (__syncthreads_or(sfail)) {
-                if (tid == 0) set_status(args.status, KDA_DEV_TIMEOUT);
+                if (tid == 0) {
+                    set_status(args.status, KDA_DEV_TIMEOUT);
+                    drain(ib, par_in, par_S);
+                }
                 return;
             }
             if (j == 0 && tid == 0) {  // the state buffer and the other input buffer are free: next item

@@ -78,6 +78,18 @@ struct ProjectArgs {
 int launch_project(const ProjectArgs &a, cudaStream_t st);
 
 bool prefill_supported(int dk, int dv, int W, int chunk);
+// The host-side argument checks of kda_prefill_chunked (everything but the workspace); KDA_OK or the failure
+// code with the reason recorded.  Makes no CUDA call.
+int check_prefill_args(const kda_pool *pool, const kda_params *prm, int32_t nseq, int64_t total_tokens,
+                       const int32_t *cu_seqlens, const int64_t *start_pos, const int32_t *src_slot,
+                       const int32_t *dst_slot, int32_t chunk, int64_t ckpt_interval, const int32_t *ckpt_offsets,
+                       const int32_t *ckpt_slots, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const uint16_t *a, const uint16_t *b, const uint16_t *z, const uint16_t *y,
+                       const int32_t *dev_status);
+// One-time per-device set-up of the prefill launchers, done on the current device: kernel attributes, the
+// tensor-map encoder, the SM count, and the side stream and events of segmented launches.  Later calls do
+// nothing.  KDA_OK or KDA_ERR_CUDA.
+int prefill_prepare();
 size_t prefill_workspace_bytes(int H, int dk, int dv, int nseq, int64_t total_tokens, int chunk);
 int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st);
 

@@ -54,9 +54,15 @@ enum : int32_t { kSeqInvalid = 1, kSeqCkptBad = 2 };
 struct Layout {
     int64_t maxc;
     size_t off_cnt, off_ent, off_pos, off_seqc, off_flags;
+    size_t off_win;   // bf16 [nseq][H][W-1][2dk+dv]: the source slots' windows as they were when the call began
+    int32_t win_u4;   // 16-byte words per (sequence, head) window
     size_t off_W, off_U, off_Kt, off_Qp, off_Qk, off_gl, off_O;
     size_t total;
 };
+
+// 16-byte words of one stored conv window ([W-1][2dk+dv] bf16; a whole number of words for every supported
+// shape, whose dk and dv are multiples of 16).
+inline int32_t window_u4(int dk, int dv) { return (int32_t)((kConvW - 1) * (2 * dk + dv) * 2 / 16); }
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -69,6 +75,8 @@ Layout make_layout(int H, int dk, int dv, int nseq, int64_t T, int C) {
     L.off_pos = o; o = align256(o + sizeof(int64_t) * L.maxc);
     L.off_seqc = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
     L.off_flags = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
+    L.win_u4 = window_u4(dk, dv);
+    L.off_win = o; o = align256(o + (size_t)16 * L.win_u4 * nseq * H);
     const size_t per = (size_t)L.maxc * H;
     L.off_W = o; o = align256(o + 4 * per * C * dk);
     L.off_U = o; o = align256(o + 4 * per * C * dv);
@@ -106,21 +114,40 @@ __device__ __forceinline__ uint16_t raw_bits(const PrefillArgs &a, int dk, int d
 }
 
 // Raw bits of channel ch at absolute position pos of sequence n (pos >= start - (W-1)): from this
-// call's tokens when pos >= start, else from the source slot's stored window (zeros for src = -1).
+// call's tokens when pos >= start, else from the source window as it was when the call began (`win`, the
+// sequence's snapshot for this head; zeros for src = -1).
 __device__ __forceinline__ uint16_t raw_at(const PrefillArgs &a, int dk, int dv, int h, int ch, int64_t pos,
-                                           int64_t start, int64_t ts, int src) {
+                                           int64_t start, int64_t ts, int src, const uint16_t *win) {
     if (pos >= start) return raw_bits(a, dk, dv, ts + (pos - start), h, ch);
     if (src < 0) return 0;
     const int CC = 2 * dk + dv;
     const int row = (int)(pos - start + (kConvW - 1));
-    return a.conv[(((size_t)src * a.H + h) * (kConvW - 1) + row) * CC + ch];
+    return win[row * CC + ch];
 }
 
 // ------------------------------------------------------------------------------------------ 1. table
+// Block 0 validates the tables and builds the chunk table.  The other blocks copy each sequence's source
+// window (src >= 0) into the workspace: the intra kernels read a sequence's history rows from that copy,
+// never from the pool, so an in-place call (src == dst) cannot see the destination window that the item of
+// the sequence's last chunk writes, whichever CTA runs first.
 __global__ void __launch_bounds__(kMaxSeqThreads) prefill_table_kernel(const PrefillArgs a, const Layout L) {
     __shared__ int32_t scan[kMaxSeqThreads];
     __shared__ int32_t carry_s;
     const int tid = threadIdx.x;
+    if (blockIdx.x > 0) {
+        const int64_t words = (int64_t)a.nseq * a.H * L.win_u4;
+        uint4 *snap = wsp<uint4>(a, L.off_win);
+        const uint4 *pool = reinterpret_cast<const uint4 *>(a.conv);
+        for (int64_t w = (int64_t)(blockIdx.x - 1) * kMaxSeqThreads + tid; w < words;
+             w += (int64_t)(gridDim.x - 1) * kMaxSeqThreads) {
+            const int64_t unit = w / L.win_u4, n = unit / a.H;
+            const int h = (int)(unit - n * a.H);
+            const int src = a.src[n];
+            if (src >= 0 && src < a.num_slots)  // range-checked here too: block 0 validates concurrently
+                snap[w] = pool[((int64_t)src * a.H + h) * L.win_u4 + (w - unit * L.win_u4)];
+        }
+        return;
+    }
     const int C = a.chunk;
     int32_t *cnt = wsp<int32_t>(a, L.off_cnt);
     int32_t *seqc = wsp<int32_t>(a, L.off_seqc);
@@ -211,6 +238,7 @@ __global__ void __launch_bounds__(kThreads) prefill_intra_kernel(const PrefillAr
     const int64_t start = a.start_pos[n], ts = a.cu_seqlens[n];
     const int64_t len = (int64_t)a.cu_seqlens[n + 1] - ts;
     const int srcv = a.src[n];  // validated by the table kernel (sequences with bad slots have no chunks)
+    const uint16_t *win = wsp<uint16_t>(a, L.off_win) + ((size_t)n * H + h) * L.win_u4 * 8;
 
     float *qh = sm;                // [C][dk]
     float *kh = qh + C * dk;       // [C][dk]
@@ -223,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) prefill_intra_kernel(const PrefillAr
     // causal conv + SiLU, one channel per thread, sequential over the chunk's tokens
     for (int ch = tid; ch < CC; ch += kThreads) {
         float hist[kConvW - 1];
-        for (int j = 0; j < kConvW - 1; ++j) hist[j] = bf2f(raw_at(a, dk, dv, h, ch, p0 - (kConvW - 1) + j, start, ts, srcv));
+        for (int j = 0; j < kConvW - 1; ++j) hist[j] = bf2f(raw_at(a, dk, dv, h, ch, p0 - (kConvW - 1) + j, start, ts, srcv, win));
         const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
         for (int r = 0; r < C; ++r) {
             float out = 0.f;
@@ -338,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) prefill_intra_kernel(const PrefillAr
         uint16_t *cw = a.conv + ((size_t)wslot[w] * H + h) * (kConvW - 1) * CC;
         for (int idx = tid; idx < (kConvW - 1) * CC; idx += kThreads) {
             const int row = idx / CC, ch = idx - (idx / CC) * CC;
-            cw[idx] = raw_at(a, dk, dv, h, ch, pend - (kConvW - 1) + row, start, ts, srcv);
+            cw[idx] = raw_at(a, dk, dv, h, ch, pend - (kConvW - 1) + row, start, ts, srcv, win);
         }
     }
 }
@@ -467,9 +495,14 @@ __global__ void __launch_bounds__(kThreads) prefill_out_kernel(const PrefillArgs
 //   [A ; Qk]  = [K+ ; Q+] (mid-chunk reference) x K-^T           tf32, M=128 N=64  K=128 (two halves)
 //   W^T       = (k*exp(G))^T x T^T,   U'^T = V^T x T^T            tf32, M=128 N=64  K=64
 //   U^T       = U'^T + S^T x (-W)^T                                bf16, M=128 N=64  K=128
-//   O^T       = S^T x Q+^T + U^T x Qk^T                            bf16, M=128 N=64  K=128 / 64
+//   O^T       = S^T x Q+^T                                         bf16, M=128 N=64  K=128
+//             + U^T x Qk^T                                         tf32, M=128 N=64  K=64
 //   S^T       = S^T Diag(exp(G_last)) + U^T x Ktil                 tf32, M=128 N=128 K=64
-// tf32 operands are rounded to nearest (cvt.rna); accumulation is fp32 in tensor memory.
+// tf32 operands are rounded to nearest (cvt.rna); accumulation is fp32 in tensor memory.  The diagonal of
+// Qk is not taken from the MMA: it is scale * (q^_r . k^_r), summed in fp32 from the normalised vectors.
+// Where q^_r and k^_r are nearly orthogonal (a sequence's first token from an empty state makes O_r that
+// single term) the rounded operands of the MMA would lose the dot product's relative accuracy, and the
+// gated RMSNorm scales the output back up to unit size.
 namespace tc {
 
 constexpr int D = 128, CH = 64;
@@ -477,8 +510,8 @@ constexpr float kMidRange = 40.f;  // |G_r - G_mid| bound for the factorised A /
 
 // Workspace block per (chunk, head); the first WS_OPS bytes are operand tiles in their shared-memory
 // layout (K-major, 128B swizzle), copied verbatim by the state kernel.
-constexpr uint32_t WS_QK = 0;                    // bf16 [64 r][64 s]    Qk (scaled, masked)
-constexpr uint32_t WS_W = WS_QK + CH * CH * 2;   // bf16 [64 r][128 i]   -W (negated)
+constexpr uint32_t WS_QK = 0;                    // tf32 [64 r][64 s]    Qk (scaled, masked, fp32 diagonal)
+constexpr uint32_t WS_W = WS_QK + CH * CH * 4;   // bf16 [64 r][128 i]   -W (negated)
 constexpr uint32_t WS_QP = WS_W + CH * D * 2;    // bf16 [64 r][128 i]   scale * q * exp(G)
 constexpr uint32_t WS_KT = WS_QP + CH * D * 2;   // tf32 [128 i][64 r]   k * exp(G_last - G), transposed
 constexpr uint32_t WS_GL = WS_KT + D * CH * 4;   // fp32 [128]           exp(G_last)
@@ -490,7 +523,7 @@ static_assert(WS_OPS % 16 == 0, "bulk copy size");
 
 struct Layout2 {
     int64_t maxc;
-    size_t off_cnt, off_ent, off_pos, off_seqc, off_flags, off_blk, off_carry, total;
+    size_t off_cnt, off_ent, off_pos, off_seqc, off_flags, off_win, off_blk, off_carry, total;
 };
 
 inline Layout2 make_layout2(int H, int nseq, int64_t T) {
@@ -502,6 +535,7 @@ inline Layout2 make_layout2(int H, int nseq, int64_t T) {
     L.off_pos = o; o = align256(o + sizeof(int64_t) * L.maxc);
     L.off_seqc = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
     L.off_flags = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
+    L.off_win = o; o = align256(o + (size_t)16 * window_u4(D, D) * nseq * H);
     o = (o + 1023) & ~size_t(1023);
     L.off_blk = o; o += (size_t)WS_BLOCK * L.maxc * H;
     L.off_carry = o; o += (size_t)nseq * H * D * D * 4;  // fp32 state of each (sequence, head) between segments
@@ -514,6 +548,7 @@ inline Layout as_layout(const Layout2 &L2) {  // the table kernel only uses thes
     L.maxc = L2.maxc;
     L.off_cnt = L2.off_cnt; L.off_ent = L2.off_ent; L.off_pos = L2.off_pos;
     L.off_seqc = L2.off_seqc; L.off_flags = L2.off_flags;
+    L.off_win = L2.off_win; L.win_u4 = window_u4(D, D);
     return L;
 }
 
@@ -526,20 +561,22 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 //   P0-P1  [0,32K) q^ fp32 | [32K,64K) k^ fp32 | [64K,96K) G fp32 (decay logits staged in its first 16K) |
 //          [96K,128K) V^T tf32 tile | [128K,180K) raw rows
 //   P2     [128K,160K) [K+;Q+] tf32 tile | [160K,176K) K- tf32 tile (one channel half at a time)
-//   P3-P4  [0,8K) Qk staging, then [0,17K) Inv fp32 (row stride 68) | [128K,145K) A fp32 (row stride 68) | [160K,176K) block temps,
-//          then T tf32
+//   P3-P4  [0,16K) Qk tf32 staging, then [0,17K) Inv fp32 (row stride 68) | [128K,145K) A fp32 (row stride 68) |
+//          [160K,176K) block temps, then T tf32 (the wide-decay path stages Qk here instead: q^ is still read)
 //   P5     [0,32K) (k exp G)^T tf32 tile | [128K,160K) Ktil^T tf32 staging
 //   P6     [32K,48K) -W bf16 staging | [64K,96K) U' fp32 staging
 constexpr uint32_t I_Q = 0, I_K = 32768, I_G = 65536, I_VT = 98304, I_RAW = 131072;
 constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_T = 163840;
 constexpr uint32_t I_INV = 0;          // Inv fp32 [64][IST] over q^ (free after the Qk copy-out)
-constexpr uint32_t I_QKS_SLOW = 148480; // Qk staging of the wide-decay path (q^ is still read there)
-constexpr uint32_t I_MISC = 184320;   // beta, exp(G_mid), decay partial sums, barrier, tmem address, window stash
+constexpr uint32_t I_QKS_SLOW = I_T;   // Qk staging of the wide-decay path (q^ is still read there; K- is unused)
+constexpr uint32_t I_MISC = 184320;   // beta, exp(G_mid), decay partial sums, barrier, tmem address, window stash,
+                                      // fp32 q^.k^ per row
 constexpr uint32_t I_SMEM = I_MISC + 7168 + 1024;  // + alignment slack
 constexpr int RAW_ROWS = CH + kConvW - 1;           // 3 history rows + 64 tokens
 constexpr int AST = 68;                             // row stride of A in smem (padded against bank conflicts)
 constexpr int IST = 68;                             // row stride of Inv in smem (the same padding)
-static_assert(I_A + CH * AST * 4 <= I_QKS_SLOW && I_QKS_SLOW + CH * CH * 2 <= I_T, "A and slow Qk staging");
+static_assert(I_A + CH * AST * 4 <= I_T && I_QKS_SLOW + CH * CH * 4 <= I_MISC, "A and slow Qk staging");
+static_assert(I_Q + CH * CH * 4 <= I_K, "Qk staging over q^");
 static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
 static_assert(I_INV + CH * IST * 4 <= I_K && (IST * 4) % 16 == 0, "Inv staging");
 
@@ -598,6 +635,7 @@ __global__ void __launch_bounds__(NTI, 1)
     uint64_t *bar_in = bar + 1;
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + I_MISC + 3136);
     uint4 *wstash = reinterpret_cast<uint4 *>(sm + I_MISC + 3200);  // raw rows of the window after the chunk
+    float *qkd = reinterpret_cast<float *>(sm + I_MISC + 5632);      // [64] q^_r . k^_r in fp32
 
     // Item metadata from global memory (one thread; dependent loads).
     auto load_meta = [&](int item, ItemMeta *m) {
@@ -655,16 +693,16 @@ __global__ void __launch_bounds__(NTI, 1)
     if (!ok) break;  // the loads stay in flight: the exit path waits for them once more
     ph_in ^= 1;
     if (tid == 0) in_flight = false;
-    {   // history rows before the sequence start: the source slot's stored window, or zeros
+    {   // history rows before the sequence start: the source window as it was when the call began (the
+        // table kernel's snapshot), or zeros
         const ItemMeta mt = meta[it & 1];
         const int hist_src = (int)min((int64_t)(kConvW - 1), max((int64_t)0, mt.start - mt.p0 + (kConvW - 1)));
+        const uint16_t *win = wsp<uint16_t>(a, L.off_win) + ((size_t)mt.seq * H + h) * (kConvW - 1) * CC;
         for (int idx = tid; idx < hist_src * CC; idx += NTI) {
             const int row = idx / CC, ch = idx - (idx / CC) * CC;
             const int64_t p = mt.p0 - (kConvW - 1) + row;
             raw[(ch >> 7) * RAW_PART + row * D + (ch & 127)] =
-                mt.srcv >= 0
-                    ? a.conv[(((size_t)mt.srcv * H + h) * (kConvW - 1) + (p - mt.start + (kConvW - 1))) * CC + ch]
-                    : (uint16_t)0;
+                mt.srcv >= 0 ? win[(p - mt.start + (kConvW - 1)) * CC + ch] : (uint16_t)0;
         }
     }
     if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(blogit)) : 0.f;
@@ -732,16 +770,30 @@ __global__ void __launch_bounds__(NTI, 1)
                 sq[k4] += __shfl_xor_sync(0xffffffffu, sq[k4], o);
                 sk[k4] += __shfl_xor_sync(0xffffffffu, sk[k4], o);
             }
+        float dqk[4];  // q^_r . k^_r of the stored (normalised, fp32) vectors; rows past the chunk's end are 0
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
             const int r = warp + 16 * k4;
-            if (r >= ntok) continue;
             const float rq = rsqrtf(sq[k4] + a.l2_eps), rk = rsqrtf(sk[k4] + a.l2_eps);
+            float dd = 0.f;
 #pragma unroll
             for (int i = 0; i < D / 32; ++i) {
-                qh[r * D + lane + 32 * i] = vq[k4][i] * rq;
-                kh[r * D + lane + 32 * i] = vk[k4][i] * rk;
+                const float qn = vq[k4][i] * rq, kn = vk[k4][i] * rk;
+                dd = fmaf(qn, kn, dd);
+                if (r < ntok) {
+                    qh[r * D + lane + 32 * i] = qn;
+                    kh[r * D + lane + 32 * i] = kn;
+                }
             }
+            dqk[k4] = dd;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) dqk[k4] += __shfl_xor_sync(0xffffffffu, dqk[k4], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) qkd[warp + 16 * k4] = warp + 16 * k4 < ntok ? dqk[k4] : 0.f;
         }
     }
     {   // cumulative log decay along the chunk from the staged logits: 4 threads per channel, 16 tokens each,
@@ -860,10 +912,11 @@ __global__ void __launch_bounds__(NTI, 1)
             __syncthreads();
         }
     }
-    // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with diagonal, bf16 tile) ----
+    // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with the fp32 diagonal, tf32 tile) ----
     float *A = reinterpret_cast<float *>(sm + I_A);      // [64][AST]
     float *Inv = reinterpret_cast<float *>(sm + I_INV);  // [64][IST], lower block triangle
-    // Qk tile staging: over q^ (dead) on the fast path; the slow path still reads q^, so it stages behind A
+    // Qk tile staging: over q^ (dead) on the fast path; the slow path still reads q^, so it stages in the K-
+    // region (unused there)
     uint8_t *Qks = slow ? sm + I_QKS_SLOW : sm + I_Q;
     if (ok && !slow) {
         float v[32];
@@ -882,12 +935,16 @@ __global__ void __launch_bounds__(NTI, 1)
                 }
             } else {
                 const int r = row - CH;
+                const float dg = a.scale * qkd[r];
 #pragma unroll
-                for (int t = 0; t < 32; t += 8) {
-                    float x8[8];
+                for (int t = 0; t < 32; t += 4) {
+                    float x4[4];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) x8[u] = (32 * half + t + u <= r) ? a.scale * v[t + u] : 0.f;
-                    umma::st_bf16x8(Qks, CH, r, 32 * half + t, x8);
+                    for (int u = 0; u < 4; ++u) {
+                        const int s_ = 32 * half + t + u;
+                        x4[u] = s_ < r ? a.scale * v[t + u] : (s_ == r ? dg : 0.f);
+                    }
+                    umma::st_tf32x4(Qks, CH, r, 32 * half + t, x4[0], x4[1], x4[2], x4[3]);
                 }
             }
         }
@@ -904,7 +961,7 @@ __global__ void __launch_bounds__(NTI, 1)
                 }
             }
             A[r * AST + s_] = s_ < r ? accA : 0.f;
-            umma::st_bf16(Qks, CH, r, s_, s_ <= r ? a.scale * accQ : 0.f);
+            umma::st_tf32(Qks, CH, r, s_, s_ <= r ? a.scale * accQ : 0.f);
         }
     }
     if (__syncthreads_or(!ok)) {
@@ -914,7 +971,7 @@ __global__ void __launch_bounds__(NTI, 1)
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {  // Qk tile to the workspace; the staging is reused by P4, so wait until it has been read
-        bulk_s2g(blk + WS_QK, Qks, CH * CH * 2);
+        bulk_s2g(blk + WS_QK, Qks, CH * CH * 4);
         bulk_commit();
         bulk_wait_read_all();
     }
@@ -1110,16 +1167,15 @@ namespace tc {
 // State kernel smem (bytes, from a 1024-aligned base)
 constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand of U^T = S^T (-W)^T, O^T = S^T Q+^T
 constexpr uint32_t S_OPS = 32768;     // one chunk's workspace block (Qk, -W, Q+, Ktil^T, gl, U'), WS_BLOCK bytes
-constexpr uint32_t S_UT32 = 140288;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil
-constexpr uint32_t S_UT16 = 173056;   // U^T bf16 tile [128 j][64 r]: A operand of O^T += U^T Qk^T
-constexpr uint32_t S_OST = 189440;    // O staging fp32 [64 r][OST] (row stride 132: 16-byte rows, conflict-free)
+constexpr uint32_t S_UT32 = 148480;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil, O^T += U^T Qk^T
+constexpr uint32_t S_OST = 181248;    // O staging fp32 [64 r][OST] (row stride 132: 16-byte rows, conflict-free)
 constexpr int OST = 132;
-constexpr uint32_t S_NW = 223232;     // RMSNorm weight [128]
-constexpr uint32_t S_GLN = 223744;    // exp(G_last) of the next chunk [128]
-constexpr uint32_t S_MISC = 224256;   // barriers, tensor-memory address
+constexpr uint32_t S_NW = 215040;     // RMSNorm weight [128]
+constexpr uint32_t S_GLN = 215552;    // exp(G_last) of the next chunk [128]
+constexpr uint32_t S_MISC = 216064;   // barriers, tensor-memory address
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
-static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0 && S_UT16 % 1024 == 0, "state smem layout");
-static_assert(S_OST + CH * OST * 4 <= S_NW, "state smem layout");
+static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0, "state smem layout");
+static_assert(S_UT32 + D * CH * 4 <= S_OST && S_OST + CH * OST * 4 <= S_NW, "state smem layout");
 constexpr int NTS = 384;              // warps 0-7: the state chain; warps 8-11: the output epilogue
 
 // TMEM columns: S^T [0,128), U^T [128,192), O^T [192,256)
@@ -1140,7 +1196,7 @@ __device__ __forceinline__ bool state_sync_or(bool p) {
 // The sequential chunk pass of one (sequence, head).  The state warps run the recurrence with S^T in tensor
 // memory, kept decayed by the NEXT chunk's exp(G_last) so that the chunk update is one accumulating MMA:
 //   U^T  = S^T (-W)^T                 (MMA, no accumulate)      O^T  = S^T Q+^T
-//   U    = U' + U^T read back         -> tf32 / bf16 operand tiles
+//   U    = U' + U^T read back         -> tf32 operand tile
 //   O^T += U^T Qk^T                   S^T += U^T Ktil           (MMAs; S^T already holds S^T diag(exp(G_last)))
 //   S pass: bf16 operand tile of the new S, checkpoint, then S^T diag(exp(G_last of the next chunk)) back to
 //   tensor memory (or the final state to dst).
@@ -1158,7 +1214,6 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     uint8_t *Sst = sm + S_ST;
     uint8_t *ops = sm + S_OPS;
     uint8_t *Ut32 = sm + S_UT32;
-    uint8_t *Ut16 = sm + S_UT16;
     float *Ost = reinterpret_cast<float *>(sm + S_OST);
     float *nw = reinterpret_cast<float *>(sm + S_NW);
     float *gln = reinterpret_cast<float *>(sm + S_GLN);
@@ -1197,8 +1252,8 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         bulk_g2s(ops + WS_UP, blk_of(c) + WS_UP, CH * D * 4, bar_u);
     };
     auto issue_b = [&](int32_t c) {
-        mbar_arrive_expect_tx(bar_b, CH * CH * 2 + D * CH * 4 + D * 4);
-        bulk_g2s(ops + WS_QK, blk_of(c) + WS_QK, CH * CH * 2, bar_b);
+        mbar_arrive_expect_tx(bar_b, CH * CH * 4 + D * CH * 4 + D * 4);
+        bulk_g2s(ops + WS_QK, blk_of(c) + WS_QK, CH * CH * 4, bar_b);
         bulk_g2s(ops + WS_KT, blk_of(c) + WS_KT, D * CH * 4 + D * 4, bar_b);  // Ktil^T and exp(G_last)
     };
 
@@ -1321,7 +1376,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 out_w = true;
                 par_w = ph_w;
             }
-            // ---- U = U' + U^T -> its tf32 and bf16 operand tiles ----
+            // ---- U = U' + U^T -> its tf32 operand tile ----
             const bool oku = mbar_wait(bar_u, ph_u);
             if (oku) out_u = false;
             ok = __all_sync(0xffffffffu, oku && ok);  // warp-uniform: the load is a warp operation
@@ -1339,8 +1394,6 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
 #pragma unroll
                 for (int t = 0; t < 32; t += 4)
                     umma::st_tf32x4(Ut32, D, j, 32 * half + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
-#pragma unroll
-                for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Ut16, D, j, 32 * half + t, v + t);
             }
             if (tid < D) gln[tid] = gnext;
             fence_proxy_async_smem();
@@ -1363,9 +1416,9 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                         umma::mma_tf32(tmem + T_S, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_KT, D, ks), ids,
                                        true);
                     umma::commit(bar_mma);  // the S pass needs only S^T
-                    const uint32_t ido = umma::idesc(umma::kBF16, 128, CH);
-                    for (int ks = 0; ks < CH / 16; ++ks)
-                        umma::mma_bf16(tmem + T_O, umma::sdesc_k(Ut16, D, ks), umma::sdesc_k(ops + WS_QK, CH, ks), ido,
+                    const uint32_t ido = umma::idesc(umma::kTF32, 128, CH);
+                    for (int ks = 0; ks < CH / 8; ++ks)
+                        umma::mma_tf32(tmem + T_O, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_QK, CH, ks), ido,
                                        true);
                     umma::commit(bar_o);    // covers both rounds of O^T MMAs
                 }
@@ -1528,6 +1581,13 @@ size_t prefill_workspace_bytes(int H, int dk, int dv, int nseq, int64_t total_to
     return make_layout(H, dk, dv, nseq, total_tokens, chunk).total;
 }
 
+// Blocks of the table kernel: one for the tables, and enough for the window snapshot (at most two per SM).
+static unsigned table_grid(const PrefillArgs &a, const Layout &L) {
+    const long long words = (long long)a.nseq * a.H * L.win_u4;
+    const long long copy = std::min<long long>((words + kMaxSeqThreads - 1) / kMaxSeqThreads, 2LL * current_device_sms());
+    return (unsigned)(1 + copy);
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -1580,24 +1640,55 @@ static SideStream *side_stream(int dev) {
     return &side[dev];
 }
 
+// The dynamic shared-memory limits of the prefill kernels, once per device (the current one).
+static int set_prefill_attributes(int dev) {
+    static std::atomic<int> done[64];
+    if (done[dev].load(std::memory_order_acquire)) return KDA_OK;
+    const int max_smem = 227 * 1024;
+    if (cudaFuncSetAttribute(tc::prefill_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::I_SMEM) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(tc::prefill_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::S_SMEM) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(prefill_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(prefill_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+            cudaSuccess)
+        return launch_result("prefill: cudaFuncSetAttribute");
+    done[dev].store(1, std::memory_order_release);
+    return KDA_OK;
+}
+
+// The side stream and events of segmented launches on this device, created on first use (caller holds mu).
+static int ensure_side_stream(SideStream *ss) {
+    if (ss->stream) return KDA_OK;
+    if (cudaStreamCreateWithFlags(&ss->stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss->join, cudaEventDisableTiming) != cudaSuccess)
+        return launch_result("prefill: side stream creation");
+    return KDA_OK;
+}
+
+int prefill_prepare() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_result("prefill: cudaGetDevice");
+    if (set_prefill_attributes(dev) != KDA_OK) return KDA_ERR_CUDA;
+    if (!tensor_map_encoder()) return fail(KDA_ERR_CUDA, "prefill: cuTensorMapEncodeTiled is not available");
+    (void)current_device_sms();
+    SideStream *ss = side_stream(dev);
+    std::lock_guard<std::mutex> lock(ss->mu);
+    return ensure_side_stream(ss);
+}
+
 static int launch_prefill_tc(const PrefillArgs &a0, cudaStream_t st) {
     PrefillArgs a = a0;
     a.seg_lo = 0;
     a.seg_hi = INT32_MAX;
     const tc::Layout2 L2 = tc::make_layout2(a.H, a.nseq, a.total_tokens);
-    static int attr_done[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_result("prefill: cudaGetDevice");
-    if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(tc::prefill_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tc::I_SMEM) != cudaSuccess ||
-            cudaFuncSetAttribute(tc::prefill_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tc::S_SMEM) != cudaSuccess)
-            return launch_result("prefill: cudaFuncSetAttribute");
-        attr_done[dev] = 1;
-    }
+    if (set_prefill_attributes(dev) != KDA_OK) return KDA_ERR_CUDA;
     if (L2.maxc * a.H > 0x7fffffffLL || a.H > 65535) return fail(KDA_ERR_INVALID_ARG, "prefill: grid too large");
-    prefill_table_kernel<<<1, kMaxSeqThreads, 0, st>>>(a, tc::as_layout(L2));
+    prefill_table_kernel<<<table_grid(a, tc::as_layout(L2)), kMaxSeqThreads, 0, st>>>(a, tc::as_layout(L2));
     CUtensorMap tq, tk, tv, ta;
     if (a.total_tokens > 0) {
         const EncodeTiledFn enc = tensor_map_encoder();
@@ -1623,12 +1714,7 @@ static int launch_prefill_tc(const PrefillArgs &a0, cudaStream_t st) {
     SideStream *ss = side_stream(dev);
     if (!ss) return fail(KDA_ERR_CUDA, "prefill: no side stream for this device");
     std::lock_guard<std::mutex> lock(ss->mu);  // one segmented call at a time per device: the events are shared
-    if (!ss->stream) {
-        if (cudaStreamCreateWithFlags(&ss->stream, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ss->join, cudaEventDisableTiming) != cudaSuccess)
-            return launch_result("prefill: side stream creation");
-    }
+    if (ensure_side_stream(ss) != KDA_OK) return KDA_ERR_CUDA;
     const unsigned gi = (unsigned)(nsm - chains);  // the intra CTAs leave one SM to each state CTA
     bool forked = true;
     for (long long lo = 0; lo < L2.maxc && forked; lo += kSegChunks) {
@@ -1652,20 +1738,11 @@ int launch_prefill(const PrefillArgs &a, int dk, int dv, cudaStream_t st) {
     const size_t smem_intra = sizeof(float) * (3 * C * dk + C * (dk + dv) + 2 * C * C + C);
     const int DVT = std::min(dv, 32);
     const size_t smem_state = sizeof(float) * (dk * DVT + 3 * C * dk + C * C + 2 * C * DVT + dk);
-    static int attr_done[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_result("prefill: cudaGetDevice");
-    if (!attr_done[dev]) {
-        const int max_smem = 227 * 1024;
-        if (cudaFuncSetAttribute(prefill_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(prefill_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-                cudaSuccess)
-            return launch_result("prefill: cudaFuncSetAttribute");
-        attr_done[dev] = 1;
-    }
+    if (set_prefill_attributes(dev) != KDA_OK) return KDA_ERR_CUDA;
     if (L.maxc > 0x7fffffffLL || a.H > 65535) return fail(KDA_ERR_INVALID_ARG, "prefill: grid too large");
-    prefill_table_kernel<<<1, kMaxSeqThreads, 0, st>>>(a, L);
+    prefill_table_kernel<<<table_grid(a, L), kMaxSeqThreads, 0, st>>>(a, L);
     if (a.total_tokens > 0) {
         dim3 gi((unsigned)L.maxc, a.H);
         prefill_intra_kernel<<<gi, kThreads, smem_intra, st>>>(a, L, dk, dv);

@@ -116,10 +116,11 @@ __global__ void __launch_bounds__(NT, 1)
     umma::fence_after();
     const uint32_t tmem = *tmem_s;
     bool ok = true;
+    int kg = 0;  // producer: K steps whose loads were issued; MMA issuer: K steps whose MMAs were issued
 
     if (warp == 0) {
         if (lane == 0) {  // producer: TMA loads of the x and W tiles of every K step of every tile
-            int kg = 0;   // K steps issued so far (all tiles): stage kg % STAGES, use kg / STAGES
+            // K step kg (counted over all tiles) uses stage kg % STAGES for the (kg / STAGES)-th time
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 int tm, tn;
                 tile_coords(p, t, tm, tn);
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(NT, 1)
     } else if (warp == 1) {
         if (lane == 0) {  // MMA issuer: accumulator i % 2 for the i-th tile of this CTA
             const uint32_t id = umma::idesc(umma::kBF16, BM, BN);
-            int kg = 0, i = 0;
+            int i = 0;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
                 const int a2 = i & 1;
                 if (i >= 2 && !mbar_wait(acc_empty + a2, (uint32_t)(i / 2 - 1) & 1u)) {
@@ -195,6 +196,19 @@ __global__ void __launch_bounds__(NT, 1)
         }
     }
     if (!ok && lane == 0) set_status(p.status, KDA_DEV_TIMEOUT);
+    // After a timed-out wait anywhere in the CTA, loads may still be landing in its shared memory and MMAs
+    // may still be reading it and writing the accumulators: the producer waits for its last STAGES loads and
+    // the MMA issuer for the commit of its last MMAs (which covers every earlier one), briefly and bounded,
+    // before the tensor memory is freed and the CTA exits.
+    if (__syncthreads_or(!ok) && lane == 0 && warp < 2) {
+        constexpr uint64_t kDrainNs = 10000000ull;
+        if (warp == 0) {
+            for (int j = kg > STAGES ? kg - STAGES : 0; j < kg; ++j)
+                mbar_wait(full + j % STAGES, (uint32_t)(j / STAGES) & 1u, kDrainNs);
+        } else if (kg > 0) {
+            mbar_wait(empty + (kg - 1) % STAGES, (uint32_t)((kg - 1) / STAGES) & 1u, kDrainNs);
+        }
+    }
     umma::fence_before();
     __syncthreads();
     if (warp == 0) umma::dealloc(tmem, 2 * BN);

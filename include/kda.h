@@ -210,8 +210,16 @@ KDA_API int kda_prefill_chunked(const kda_pool *pool, const kda_params *prm, int
  *   Arguments: as kda_prefill_chunked, minus workspace and workspace_bytes.
  *   Limit: a problem whose kda_prefill_workspace_bytes() exceeds KDA_NOALLOC_SCRATCH_BYTES returns
  *   KDA_ERR_WORKSPACE without launching (64 MiB holds, e.g., one 512-token sequence at H = 32, dk = dv = 128).
- *   The first call on a device resolves the array's device address (cudaGetSymbolAddress) with that
- *   device current; make that first call before any stream capture on the device.
+ *   Errors: the argument checks of kda_prefill_chunked come first and make no CUDA call; then the size
+ *   check (KDA_ERR_WORKSPACE); then the per-device set-up below (KDA_ERR_CUDA if it fails).
+ *   Set-up: the first call on a device (with that device current) looks up the array's device address
+ *   (cudaGetSymbolAddress).  Under CUDA's lazy module loading that is also when the driver allocates the
+ *   array on that device, so a caller that must allocate nothing later makes this call at start-up,
+ *   before it reserves its own memory pool.  The same call does the prefill launchers' one-time set-up
+ *   (kernel attributes; the side stream and two events that segmented launches use), so later calls
+ *   create nothing.  A call with nseq = 0 does the set-up and nothing else.  Make it before any stream
+ *   capture on the device.  The address is cached per device for the life of the process; a device
+ *   reset (cudaDeviceReset) invalidates it, and the library must not be used on that device afterwards.
  *   All calls on a device share the one array and it keeps the last call's contents (nothing in it needs
  *   to start at zero): calls whose executions overlap on the GPU -- on different streams, or from
  *   different host threads -- race on it and must be serialised by the caller.

@@ -1,15 +1,18 @@
 """kda_prefill_chunked_noalloc, the prefill entry point for callers that cannot allocate device memory
 (for example an engine whose caching allocator owns all free GPU memory, or a plug-in handed only
-tensors).  It takes no workspace: the library's fixed scratch array stands in for it.
+tensors).  It takes no workspace: the library's fixed scratch array stands in for it.  It runs the same
+kernels on the same inputs as kda_prefill_chunked, so its results must be identical bit for bit; a
+tolerance would hide a stale-scratch fault.
 
 This file sorts last so that, if it fails, a run stopping at the first failure has already run every
 other test.  It must also pass alone in a fresh process.
 """
+
 import numpy as np
 import pytest
 import torch
 
-from tests.kda_testutil import S_TOL, Y_TOL, bf16_dev_bits, bf16_dev_to_f64, fill_pool, s_err, to_dev_bf16, y_err
+from tests.kda_testutil import fill_pool, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -61,12 +64,42 @@ def test_noalloc_prefill_matches_workspace_entry_point_on_two_calls():
                                         tok["z"], y, status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0, call
-        assert y_err(bf16_dev_to_f64(y), bf16_dev_to_f64(y_ref)) <= Y_TOL, call
-        for s in written:
-            assert s_err(pool.S[s].cpu().numpy(), S_ref[s].cpu().numpy()) <= S_TOL, (call, s)
-            np.testing.assert_array_equal(bf16_dev_bits(pool.conv[s]), bf16_dev_bits(C_ref[s]))
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), call
+        assert torch.equal(pool.S, S_ref), call  # written slots equal, untouched slots unchanged
+        assert torch.equal(pool.conv.view(torch.int16), C_ref.view(torch.int16)), call
         untouched = [s for s in range(24) if s not in written]
         assert torch.equal(pool.S[untouched], start_S[untouched])
+
+
+def test_noalloc_setup_call_and_argument_checks():
+    """A call with nseq = 0 does the per-device set-up and launches nothing; bad arguments are rejected with
+    KDA_ERR_INVALID_ARG by the host checks, before any device call."""
+    import hybrid_linear_attention_decode_gb300 as kda
+    lib = kda.load_library()
+    pool = kda.StatePool.empty(4, 2, 128, 128)
+    prm = kda.LayerParams(torch.zeros(2, 384, 4, device="cuda"), torch.ones(128, device="cuda"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device="cuda")  # noqa: E731
+    i32 = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")  # noqa: E731
+    # nseq = 0: the set-up call
+    kda.kda_prefill_chunked_noalloc(pool, prm, i32([0]), torch.zeros(0, dtype=torch.int64, device="cuda"),
+                                    i32([0])[:0], i32([0])[:0], 64, 0, i32([0]), i32([0]), None, None, None, None,
+                                    None, None, None, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # a NULL pool and NULL params: KDA_ERR_INVALID_ARG, whatever the sizes
+    rc = lib.kda_prefill_chunked_noalloc(None, None, 1, 64, *([None] * 4), 64, 0, *([None] * 9), None, None)
+    assert rc == kda.KDA_ERR_INVALID_ARG
+    assert "pool" in kda.kda_last_error_string() or "params" in kda.kda_last_error_string()
+    # an interval that is not a multiple of the chunk
+    with pytest.raises(kda.KdaError) as err:
+        kda.kda_prefill_chunked_noalloc(pool, prm, i32([0, 64]), torch.zeros(1, dtype=torch.int64, device="cuda"),
+                                        i32([-1]), i32([0]), 64, 100, i32([0, 0]), i32([0]), e(64, 2, 128),
+                                        e(64, 2, 128), e(64, 2, 128), e(64, 2, 128), e(64, 2), None, e(64, 2, 128),
+                                        status)
+    assert err.value.rc == kda.KDA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
 
 
 def test_noalloc_prefill_rejects_problems_beyond_the_scratch():
