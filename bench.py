@@ -145,6 +145,20 @@ def file_sha(*paths) -> str:
     return h.hexdigest()[:16]
 
 
+def profiled_values(name: str, sha: str) -> dict:
+    """The key: value lines of profiles/<name>_traffic.txt when its kernel_source_sha matches `sha`, else {}."""
+    path = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        return kv if kv.get("kernel_source_sha") == sha else {}
+    except Exception:
+        return {}
+
+
 def profiled_traffic(name: str, sha: str):
     """dram bytes per launch recorded in profiles/<name>_traffic.txt for this exact kernel source, else None."""
     path = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
@@ -396,6 +410,9 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
     e2e_val = dec_tokens * Ke / (e2e_ms / 1000.0)
 
+    # ---- the decode step at batch 64, 128 and 256: the fixed cost of a step
+    decode_sweep = run_decode_sweep(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws)
+
     # ---- the same decode step on a bf16 state pool
     decode_bf16 = run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws)
 
@@ -431,6 +448,7 @@ def run_gpu(args):
                                          "call, y copied back to pinned host memory; copies of neighbouring "
                                          "steps overlap the kernel"},
             "gpu_launches": K,
+            "decode_batch_sweep": decode_sweep,
             "decode_bf16_state": decode_bf16,
             "decode_multi_verify": decode_multi,
             "projection": projection,
@@ -484,6 +502,57 @@ def run_project(args, kda, torch, dev, stream, seed, ws):
                         f"d=128 ({N} features) in one GEMM, bf16 in, fp32 accumulate, bf16 out",
             "tokens_per_s": T * ws / (ms / 1000.0), "ms_per_call": ms, "steps": K, "tflops": tf,
             "bf16_peak_tflops": bf16_peak, "peak_kind": kind, "tensor_frac": tf / bf16_peak}
+
+
+def run_decode_sweep(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
+    """The decode step at batch 64, 128 and 256 on the decode workload's pool (fresh random slots every step,
+    one graph replay of K steps each), and a least-squares fit of time per step = fixed + per_item * items
+    (items = batch x heads): the fixed part is what a step costs beyond streaming its items."""
+    K = max(3, min(args.steps, 300))
+    rows = []
+    for N in (64, 128, 256):
+        tok = ki.token_inputs(seed + 20, N, H, DK, DV)
+        d = {k: bf16_dev(v, dev) for k, v in tok.items()}
+        y = torch.empty(N, H, DV, dtype=torch.bfloat16, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed + N)
+        sl = torch.rand(K + 3, DEC_SLOTS, device=dev, generator=g).argsort(dim=1)[:, :N].to(torch.int32).contiguous()
+
+        def dec(i, st=stream):
+            kda.kda_decode_step(pool, prm, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], y, sl[i], sl[i], status,
+                                st)
+        for i in range(3):
+            dec(i)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for i in range(K):
+                dec(3 + i, None)
+        gr.replay()
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = max_over_ranks(e0.elapsed_time(e1), ws) / K * 1000.0
+        del gr
+        if int(status.item()) != 0:
+            return {"error": f"device status {int(status.item())} at batch {N}"}
+        rows.append((N, us))
+    items = np.array([n * H for n, _ in rows], dtype=np.float64)
+    t = np.array([u for _, u in rows])
+    per_item, fixed = np.polyfit(items, t, 1)
+    per_item_bytes = DECODE_BYTES_PER_HEAD_TOKEN
+    return {"workload": "decode step at batch 64 / 128 / 256, H=32, dk=dv=128, fp32 pool of 4096 slots, fresh "
+                        "random slots per step",
+            "us_per_step": {str(n): u for n, u in rows},
+            "hbm_frac": {str(n): per_item_bytes * n * H / (u / 1e6) / 1e9 / hbm_peak for n, u in rows},
+            "fit": {"fixed_us": float(fixed), "per_item_ns": float(per_item * 1000.0),
+                    "streaming_gbs": per_item_bytes / (per_item * 1e-6) / 1e9},
+            "steps": K}
 
 
 MULTI_L = 5  # verify step: 4 draft tokens + 1
@@ -662,11 +731,44 @@ def run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, w
     if int(status.item()) != 0:
         return {"error": f"device status {int(status.item())}"}
     dec_bytes = DECODE_BYTES_PER_HEAD_TOKEN * N * H
+    pre_io = PREFILL_IO_BYTES_PER_HEAD_TOKEN * T * H + CKPT_BYTES * (nck + 1) * H
     return {"workload": f"long context: one {T}-token prefill (H=32, d=128, chunk 64, checkpoints every {I} "
                         f"tokens), then a batch-{N} decode step continuing it plus {N - 1} other slots",
             "prefill_ms": pre_ms, "prefill_tokens_per_s": T * ws / (pre_ms / 1000.0),
+            "prefill_roofline": prefill_roofline(pre_ms, T * H, pre_io, "kda_prefill_long"),
             "decode_us": dec_ms * 1000.0, "decode_tokens_per_s": N * ws / (dec_ms / 1000.0),
             "decode_hbm_frac": dec_bytes / (dec_ms / 1000.0) / 1e9 / hbm_peak}
+
+
+# Useful floating-point work of the chunked form per (token, head) at chunk C = 64, dk = dv = d = 128 (2 flops
+# per multiply-add): the intra-chunk products A, Qk, W, U' and Qk U (5 x 2 C d), the state-side products W S,
+# Q+ S and K~^T U (3 x 2 d^2), and the triangular inverse (2 C^2 / 3 per token).
+PREFILL_FLOPS_PER_HEAD_TOKEN = 5 * 2 * PRE_CHUNK * DK + 3 * 2 * DK * DV + 2 * PRE_CHUNK ** 2 / 3
+PREFILL_SOURCES = ("hybrid_linear_attention_decode_gb300/csrc/kda_prefill.cu",
+                   "hybrid_linear_attention_decode_gb300/csrc/kda_device.cuh",
+                   "hybrid_linear_attention_decode_gb300/csrc/kda_umma.cuh")
+
+
+def prefill_roofline(ms: float, head_tokens: int, algorithmic_bytes: float, profile: str) -> dict:
+    """Three views of one prefill call against the measured peaks: useful flops / bf16 peak, algorithmic bytes /
+    HBM peak, and useful flops / the rate the byte roofline allows at this arithmetic intensity; plus the
+    tensor-pipe activity and DRAM traffic of an ncu capture of the same kernels, when it matches them."""
+    hbm_peak, bf16_peak, _, kind = measured_peaks()
+    flops = PREFILL_FLOPS_PER_HEAD_TOKEN * head_tokens
+    tflops = flops / (ms / 1000.0) / 1e12
+    gbs = algorithmic_bytes / (ms / 1000.0) / 1e9
+    intensity = flops / algorithmic_bytes
+    attainable = min(bf16_peak, intensity * hbm_peak / 1000.0)
+    prof = profiled_values(profile, file_sha(*PREFILL_SOURCES))
+    num = lambda k: float(prof[k]) if k in prof else None  # noqa: E731
+    return {"bound": "hbm" if intensity * hbm_peak / 1000.0 < bf16_peak else "tensor",
+            "useful_flop_per_head_token": PREFILL_FLOPS_PER_HEAD_TOKEN, "useful_tflops": tflops,
+            "useful_flop_frac": tflops / bf16_peak, "achieved_gbs": gbs, "byte_frac": gbs / hbm_peak,
+            "flop_per_byte": intensity, "attainable_tflops": attainable, "attainable_frac": tflops / attainable,
+            "tensor_pipe_frac": {k[len("tensor_pipe_frac_"):]: float(v) for k, v in prof.items()
+                                 if k.startswith("tensor_pipe_frac_")} or None,
+            "traffic": num("dram_bytes_per_call"), "peak_bf16_tflops": bf16_peak, "peak_hbm_gbs": hbm_peak,
+            "peak_kind": kind}
 
 
 def prefill_problem(seed: int, lens, chunk: int, interval: int, num_slots: int):
@@ -723,7 +825,8 @@ def run_prefill(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws):
             "tokens_per_s": T * ws / (ms / 1000.0), "ms_per_call": ms, "steps": Kp,
             "status": int(status.item()),
             "hbm_frac_of_algorithmic_bytes": io / (ms / 1000.0) / 1e9 / hbm_peak,
-            "algorithmic_bytes_per_call": io}
+            "algorithmic_bytes_per_call": io,
+            "roofline": prefill_roofline(ms, T * H, io, "kda_prefill_varlen4")}
 
 
 def run_profile_case(args):
