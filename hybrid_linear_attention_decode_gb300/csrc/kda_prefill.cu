@@ -49,6 +49,14 @@ struct ChunkEnt {
     int32_t seq, t0, n, ord;  // sequence, first token index, tokens, chunk ordinal within the sequence
 };
 
+// Everything the tensor-core intra kernel needs to know about a chunk, written by the table kernel so that the
+// kernel fetches it with one round of loads.
+struct __align__(16) ItemMeta {
+    int32_t seq, t0, n, srcv;    // sequence, first token, tokens, source slot
+    int64_t p0, start, ts, len;  // first position, the sequence's start position, first token and length
+};
+static_assert(sizeof(ItemMeta) == 48, "three 16-byte words");
+
 enum : int32_t { kSeqInvalid = 1, kSeqCkptBad = 2 };
 
 struct Layout {
@@ -56,6 +64,7 @@ struct Layout {
     size_t off_cnt, off_ent, off_pos, off_seqc, off_flags;
     size_t off_win;   // bf16 [nseq][H][W-1][2dk+dv]: the source slots' windows as they were when the call began
     int32_t win_u4;   // 16-byte words per (sequence, head) window
+    size_t off_meta;  // ItemMeta [maxc] (tensor-core path), 0 when absent
     size_t off_W, off_U, off_Kt, off_Qp, off_Qk, off_gl, off_O;
     size_t total;
 };
@@ -77,6 +86,7 @@ Layout make_layout(int H, int dk, int dv, int nseq, int64_t T, int C) {
     L.off_flags = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
     L.win_u4 = window_u4(dk, dv);
     L.off_win = o; o = align256(o + (size_t)16 * L.win_u4 * nseq * H);
+    L.off_meta = 0;
     const size_t per = (size_t)L.maxc * H;
     L.off_W = o; o = align256(o + 4 * per * C * dk);
     L.off_U = o; o = align256(o + 4 * per * C * dv);
@@ -223,6 +233,18 @@ __global__ void __launch_bounds__(kMaxSeqThreads) prefill_table_kernel(const Pre
         e.ord = j;
         ent[c] = e;
         pos[c] = p0;
+        if (L.off_meta) {
+            ItemMeta m;
+            m.seq = n;
+            m.t0 = e.t0;
+            m.n = e.n;
+            m.srcv = a.src[n];
+            m.p0 = p0;
+            m.start = start;
+            m.ts = a.cu_seqlens[n];
+            m.len = len;
+            wsp<ItemMeta>(a, L.off_meta)[c] = m;
+        }
     }
 }
 
@@ -523,7 +545,7 @@ static_assert(WS_OPS % 16 == 0, "bulk copy size");
 
 struct Layout2 {
     int64_t maxc;
-    size_t off_cnt, off_ent, off_pos, off_seqc, off_flags, off_win, off_blk, off_carry, total;
+    size_t off_cnt, off_ent, off_pos, off_seqc, off_flags, off_win, off_meta, off_blk, off_carry, total;
 };
 
 inline Layout2 make_layout2(int H, int nseq, int64_t T) {
@@ -536,6 +558,7 @@ inline Layout2 make_layout2(int H, int nseq, int64_t T) {
     L.off_seqc = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
     L.off_flags = o; o = align256(o + sizeof(int32_t) * (nseq + 1));
     L.off_win = o; o = align256(o + (size_t)16 * window_u4(D, D) * nseq * H);
+    L.off_meta = o; o = align256(o + sizeof(ItemMeta) * L.maxc);
     o = (o + 1023) & ~size_t(1023);
     L.off_blk = o; o += (size_t)WS_BLOCK * L.maxc * H;
     L.off_carry = o; o += (size_t)nseq * H * D * D * 4;  // fp32 state of each (sequence, head) between segments
@@ -548,7 +571,7 @@ inline Layout as_layout(const Layout2 &L2) {  // the table kernel only uses thes
     L.maxc = L2.maxc;
     L.off_cnt = L2.off_cnt; L.off_ent = L2.off_ent; L.off_pos = L2.off_pos;
     L.off_seqc = L2.off_seqc; L.off_flags = L2.off_flags;
-    L.off_win = L2.off_win; L.win_u4 = window_u4(D, D);
+    L.off_win = L2.off_win; L.win_u4 = window_u4(D, D); L.off_meta = L2.off_meta;
     return L;
 }
 
@@ -561,22 +584,22 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 //   P0-P1  [0,32K) q^ fp32 | [32K,64K) k^ fp32 | [64K,96K) G fp32 (decay logits staged in its first 16K) |
 //          [96K,128K) V^T tf32 tile | [128K,180K) raw rows
 //   P2     [128K,160K) [K+;Q+] tf32 tile | [160K,176K) K- tf32 tile (one channel half at a time)
-//   P3-P4  [0,16K) Qk tf32 staging, then [0,17K) Inv fp32 (row stride 68) | [128K,145K) A fp32 (row stride 68) |
-//          [160K,176K) block temps, then T tf32 (the wide-decay path stages Qk here instead: q^ is still read)
+//   P2 also writes, on the fast path, fp32 K+ = k^ exp(G - G_mid) over k^ and K- = k^ exp(G_mid - G) over G
+//   P3-P4  [188K,204K) Qk tf32 staging (its copy-out is read by the end of the item) | [0,17K) Inv fp32 (row
+//          stride 68) | [128K,145K) A fp32 (row stride 68) | [160K,176K) block temps, then T tf32
 //   P5     [0,32K) (k exp G)^T tf32 tile | [128K,160K) Ktil^T tf32 staging
-//   P6     [32K,48K) -W bf16 staging | [64K,96K) U' fp32 staging
+//   P6     [32K,48K) -W bf16 staging | [96K,128K) U' fp32 staging (both copied out by the start of the next item)
 constexpr uint32_t I_Q = 0, I_K = 32768, I_G = 65536, I_VT = 98304, I_RAW = 131072;
 constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_T = 163840;
 constexpr uint32_t I_INV = 0;          // Inv fp32 [64][IST] over q^ (free after the Qk copy-out)
-constexpr uint32_t I_QKS_SLOW = I_T;   // Qk staging of the wide-decay path (q^ is still read there; K- is unused)
 constexpr uint32_t I_MISC = 184320;   // beta, exp(G_mid), decay partial sums, barrier, tmem address, window stash,
-                                      // fp32 q^.k^ per row
-constexpr uint32_t I_SMEM = I_MISC + 7168 + 1024;  // + alignment slack
+                                      // fp32 q^.k^ per row, G_mid, exp(G_last - G_mid)
+constexpr uint32_t I_QKS = 192512;    // Qk tf32 staging [64][64]
+constexpr uint32_t I_SMEM = I_QKS + CH * CH * 4 + 1024;  // + alignment slack
 constexpr int RAW_ROWS = CH + kConvW - 1;           // 3 history rows + 64 tokens
 constexpr int AST = 68;                             // row stride of A in smem (padded against bank conflicts)
 constexpr int IST = 68;                             // row stride of Inv in smem (the same padding)
-static_assert(I_A + CH * AST * 4 <= I_T && I_QKS_SLOW + CH * CH * 4 <= I_MISC, "A and slow Qk staging");
-static_assert(I_Q + CH * CH * 4 <= I_K, "Qk staging over q^");
+static_assert(I_A + CH * AST * 4 <= I_T && I_MISC + 7168 <= I_QKS && I_QKS % 1024 == 0, "A, misc, Qk staging");
 static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
 static_assert(I_INV + CH * IST * 4 <= I_K && (IST * 4) % 16 == 0, "Inv staging");
 
@@ -584,11 +607,6 @@ constexpr int NTI = 512;  // intra kernel threads
 constexpr int RAW_PART = RAW_ROWS * D;  // elements of one raw block ([67][128] bf16 of q, k or v)
 static_assert((RAW_PART * 2) % 128 == 0, "raw blocks stay 128-byte aligned");
 
-// What the intra kernel needs to know about one work item beyond (chunk, head).
-struct ItemMeta {
-    int32_t seq, t0, n, srcv;    // sequence, first token, tokens, source slot
-    int64_t p0, start, ts, len;  // first position, the sequence's start position, first token and length
-};
 
 // Tiled TMA load of a (channel, head, token) box of a [T][H][128] bf16 token tensor into shared memory,
 // completion counted on `bar`.  The channel coordinate is always 0; token coordinates outside [0, T) read
@@ -636,19 +654,18 @@ __global__ void __launch_bounds__(NTI, 1)
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + I_MISC + 3136);
     uint4 *wstash = reinterpret_cast<uint4 *>(sm + I_MISC + 3200);  // raw rows of the window after the chunk
     float *qkd = reinterpret_cast<float *>(sm + I_MISC + 5632);      // [64] q^_r . k^_r in fp32
+    float *gmid = reinterpret_cast<float *>(sm + I_MISC + 5888);     // [128] G_mid
+    float *eglm = reinterpret_cast<float *>(sm + I_MISC + 6400);     // [128] exp(G_last - G_mid)
 
     // Item metadata from global memory (one thread; dependent loads).
+    // Item metadata: the table kernel's record of the item's chunk (one round of three 16-byte loads).
     auto load_meta = [&](int item, ItemMeta *m) {
-        const int c = item / H;
-        const ChunkEnt e = wsp<ChunkEnt>(a, L.off_ent)[c];
-        m->seq = e.seq;
-        m->t0 = e.t0;
-        m->n = e.n;
-        m->p0 = wsp<int64_t>(a, L.off_pos)[c];
-        m->start = a.start_pos[e.seq];
-        m->ts = a.cu_seqlens[e.seq];
-        m->len = (int64_t)a.cu_seqlens[e.seq + 1] - m->ts;
-        m->srcv = a.src[e.seq];
+        const uint4 *rec = reinterpret_cast<const uint4 *>(wsp<ItemMeta>(a, L.off_meta) + item / H);
+        const uint4 r0 = __ldg(rec), r1 = __ldg(rec + 1), r2 = __ldg(rec + 2);
+        uint4 *d = reinterpret_cast<uint4 *>(m);
+        d[0] = r0;
+        d[1] = r1;
+        d[2] = r2;
     };
     // TMA loads of an item's rows: 67 token rows of q, k and v starting 3 tokens before the chunk (zeros
     // before the first token), and separately (its region frees later) the chunk's 64 rows of decay logits.
@@ -686,9 +703,7 @@ __global__ void __launch_bounds__(NTI, 1)
     const bool has_next = next < total;
     const int ntok = meta[it & 1].n;
     uint8_t *blk = reinterpret_cast<uint8_t *>(a.ws) + L.off_blk + ((size_t)c * H + h) * WS_BLOCK;
-    // conv weights of this head (fetched here rather than carried from the item before: registers)
-    const float4 w = tid < CC ? __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + tid) * kConvW))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid == 0) bulk_wait_read_all();  // the item before's -W and U' copy-outs: their staging is rewritten below
     ok = !__syncthreads_or(!mbar_wait(bar_in, ph_in));
     if (!ok) break;  // the loads stay in flight: the exit path waits for them once more
     ph_in ^= 1;
@@ -707,32 +722,36 @@ __global__ void __launch_bounds__(NTI, 1)
     }
     if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(blogit)) : 0.f;
     __syncthreads();
-    // ---- P1: causal conv + SiLU, one channel per thread along the chunk (window in registers) ----
-    if (tid == NTI - 1 && has_next) load_meta(next, &meta[(it + 1) & 1]);  // warp 15 has no channel to convolve
-    if (tid < CC) {
-        const int ch = tid;
-        const uint16_t *rc = raw + (ch >> 7) * RAW_PART + (ch & 127);  // this channel's column of its block
+    // ---- P1: causal conv + SiLU over (channel, block of 16 rows) units, three per thread: the block's three
+    //      history rows come from the staged raw rows, the window runs in registers along the block ----
+#pragma unroll 1
+    for (int u = tid; u < CC * 4; u += NTI) {
+        const int ch = u % CC, rb = u / CC;
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
+        const uint16_t *rc = raw + (ch >> 7) * RAW_PART + (ch & 127) + 16 * rb * D;  // raw row 16 rb = position -3
         float h0 = bf2f(rc[0]), h1 = bf2f(rc[D]), h2 = bf2f(rc[2 * D]);
-        for (int r0 = 0; r0 < CH; r0 += 8) {
+#pragma unroll
+        for (int r8 = 0; r8 < 16; r8 += 8) {
+            const int r0 = 16 * rb + r8;
             float xs8[8], ob[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) xs8[u] = bf2f(rc[(r0 + u + 3) * D]);  // all taps before any store
+            for (int k = 0; k < 8; ++k) xs8[k] = bf2f(rc[(r8 + k + 3) * D]);  // all taps before any store
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float x = xs8[u];
+            for (int k = 0; k < 8; ++k) {
+                const float x = xs8[k];
                 float out = fmaf(w.w, x, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
                 if (a.silu) out = __fdividef(out, 1.f + __expf(-out));
-                ob[u] = (r0 + u < ntok) ? out : 0.f;
+                ob[k] = (r0 + k < ntok) ? out : 0.f;
                 h0 = h1;
                 h1 = h2;
                 h2 = x;
             }
             if (ch < D) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) qh[(r0 + u) * D + ch] = ob[u];
+                for (int k = 0; k < 8; ++k) qh[(r0 + k) * D + ch] = ob[k];
             } else if (ch < 2 * D) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) kh[(r0 + u) * D + ch - D] = ob[u];
+                for (int k = 0; k < 8; ++k) kh[(r0 + k) * D + ch - D] = ob[k];
             } else {
                 umma::st_tf32x4(Vt, D, ch - 2 * D, r0, ob[0], ob[1], ob[2], ob[3]);
                 umma::st_tf32x4(Vt, D, ch - 2 * D, r0 + 4, ob[4], ob[5], ob[6], ob[7]);
@@ -823,6 +842,8 @@ __global__ void __launch_bounds__(NTI, 1)
         const float g0 = G[tid], gm = G[MID * D + tid], gl = G[(CH - 1) * D + tid];
         wide = (g0 - gm > kMidRange) || (gm - gl > kMidRange);
         eGm[tid] = expf(gm);
+        gmid[tid] = gm;
+        eglm[tid] = expf(gl - gm);
         reinterpret_cast<float *>(blk + WS_GL)[tid] = expf(gl);
     }
     const bool slow = __syncthreads_or(wide) != 0;
@@ -837,7 +858,7 @@ __global__ void __launch_bounds__(NTI, 1)
         float xk[4][2], xq[4][2], xm[4][2];  // K+, Q+ (mid reference), K- of the thread's rows and channels
         auto form = [&](int hh) {  // ... of channel half hh; Q+ (chunk start) of that half to the workspace
             const int ic = 64 * hh + c2;
-            const float2 m2 = *reinterpret_cast<const float2 *>(G + MID * D + ic);
+            const float2 m2 = *reinterpret_cast<const float2 *>(gmid + ic);  // (row MID of G is overwritten below)
             const float2 e2 = *reinterpret_cast<const float2 *>(eGm + ic);
             const float gmv[2] = {m2.x, m2.y}, egv[2] = {e2.x, e2.y};
 #pragma unroll
@@ -866,6 +887,10 @@ __global__ void __launch_bounds__(NTI, 1)
                 }
                 *reinterpret_cast<uint32_t *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, ic)) =
                     umma::pack_bf16(xp[0], xp[1]);
+                if (!slow) {  // fp32 K+ and K- for P5, over the k^ and G they were formed from
+                    *reinterpret_cast<float2 *>(kh + r * D + ic) = make_float2(xk[j][0], xk[j][1]);
+                    *reinterpret_cast<float2 *>(G + r * D + ic) = make_float2(xm[j][0], xm[j][1]);
+                }
             }
         };
         auto store = [&]() {
@@ -915,9 +940,7 @@ __global__ void __launch_bounds__(NTI, 1)
     // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with the fp32 diagonal, tf32 tile) ----
     float *A = reinterpret_cast<float *>(sm + I_A);      // [64][AST]
     float *Inv = reinterpret_cast<float *>(sm + I_INV);  // [64][IST], lower block triangle
-    // Qk tile staging: over q^ (dead) on the fast path; the slow path still reads q^, so it stages in the K-
-    // region (unused there)
-    uint8_t *Qks = slow ? sm + I_QKS_SLOW : sm + I_Q;
+    uint8_t *Qks = sm + I_QKS;  // Qk tile staging (read by the copy-out before the next item rewrites it)
     if (ok && !slow) {
         float v[32];
         const int quad = warp & 3, half = (warp >> 2) & 1;  // warps 0-7: lanes 32*quad.., columns 32*half..
@@ -964,18 +987,15 @@ __global__ void __launch_bounds__(NTI, 1)
             umma::st_tf32(Qks, CH, r, s_, s_ <= r ? a.scale * accQ : 0.f);
         }
     }
+    fence_proxy_async_smem();  // the Qk staging is read by the async proxy below
     if (__syncthreads_or(!ok)) {
         ok = false;
         break;
     }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {  // Qk tile to the workspace; the staging is reused by P4, so wait until it has been read
+    if (tid == 0) {  // Qk tile to the workspace
         bulk_s2g(blk + WS_QK, Qks, CH * CH * 4);
         bulk_commit();
-        bulk_wait_read_all();
     }
-    __syncthreads();
     // ---- P4: T = (I + diag(beta) A)^{-1} diag(beta), blocked by 16 ----
     // L = I + diag(beta) A; Inv = L^{-1}, of which only the lower block triangle is formed (the blocks above
     // the diagonal are zero).  Diagonal 16x16 blocks by substitution, one column per thread.
@@ -1053,13 +1073,22 @@ __global__ void __launch_bounds__(NTI, 1)
     uint8_t *Kts = sm + I_A;
     for (int idx = tid; idx < D * 16; idx += NTI) {
         const int i = idx & 127, r0 = (idx >> 7) * 4;
-        const float glast = G[(CH - 1) * D + i];
         float kp[4], kt[4];
+        if (!slow) {  // k exp(G) = K+ exp(G_mid), k exp(G_last - G) = K- exp(G_last - G_mid)
+            const float em = eGm[i], el = eglm[i];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float g = G[(r0 + u) * D + i], k_ = kh[(r0 + u) * D + i];
-            kp[u] = k_ * __expf(g);
-            kt[u] = k_ * __expf(glast - g);
+            for (int u = 0; u < 4; ++u) {
+                kp[u] = kh[(r0 + u) * D + i] * em;
+                kt[u] = G[(r0 + u) * D + i] * el;
+            }
+        } else {
+            const float glast = G[(CH - 1) * D + i];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float g = G[(r0 + u) * D + i], k_ = kh[(r0 + u) * D + i];
+                kp[u] = k_ * __expf(g);
+                kt[u] = k_ * __expf(glast - g);
+            }
         }
         umma::st_tf32x4(Kpt, D, i, r0, kp[0], kp[1], kp[2], kp[3]);
         umma::st_tf32x4(Kts, D, i, r0, kt[0], kt[1], kt[2], kt[3]);
@@ -1081,13 +1110,14 @@ __global__ void __launch_bounds__(NTI, 1)
         bulk_s2g(blk + WS_KT, Kts, D * CH * 4);
         bulk_commit();
     }
+    if (tid == NTI - 1 && has_next) load_meta(next, &meta[(it + 1) & 1]);  // while every warp waits for the MMAs
     ok = wait_all(bar, phase);
     phase ^= 1;
     umma::fence_after();
     if (!ok) break;
     // ---- P6: -W (bf16 tile [64 r][128 i]) and U' (fp32 [64 r][128 j]) via smem staging ----
     uint8_t *Wst = sm + I_K;
-    float *Ust = reinterpret_cast<float *>(sm + I_G);
+    float *Ust = reinterpret_cast<float *>(sm + I_VT);  // the V^T tile is dead once the P5 MMAs are done
     if (warp < 8) {
         const int quad = warp & 3, half = warp >> 2;
         const int row = 32 * quad + lane;  // channel i (for W^T) / j (for U'^T)
@@ -1103,23 +1133,21 @@ __global__ void __launch_bounds__(NTI, 1)
     umma::fence_before();
     __syncthreads();
     // The next item's loads start here: its rows go to the raw region (every MMA is done and, once the
-    // Ktil^T copy has been read, nothing else lives there); its decay logits go to the G region once the U'
-    // copy below has read it.  Its beta logit is fetched into a register meanwhile.
+    // Ktil^T and Qk copies have been read, nothing else lives there) and its decay logits to the G region
+    // (dead after P5).  The -W and U' copy-outs are waited for at the start of the next item.  Its beta logit
+    // is fetched into a register meanwhile.
     const ItemMeta mn = meta[(it + 1) & 1];
     const int hn = next % H;
     if (tid == 0) {
         if (has_next) {
-            bulk_wait_read_all();  // the Ktil^T copy
+            bulk_wait_read_all();  // the Ktil^T and Qk copies
             issue_rows(mn, hn);
+            issue_logits(mn, hn);
+            in_flight = true;
         }
         bulk_s2g(blk + WS_W, Wst, CH * D * 2);  // -W and U' to the workspace
         bulk_s2g(blk + WS_UP, Ust, CH * D * 4);
         bulk_commit();
-        bulk_wait_read_all();
-        if (has_next) {
-            issue_logits(mn, hn);
-            in_flight = true;
-        }
     }
     if (has_next) {
         blogit = (tid < CH && tid < mn.n) ? a.b[(size_t)(mn.t0 + tid) * H + hn] : (uint16_t)0;
@@ -1151,6 +1179,7 @@ __global__ void __launch_bounds__(NTI, 1)
     }
     __syncthreads();  // the window stash and this item's metadata are rewritten by the next item
     }  // item loop
+    if (tid == 0) bulk_wait_all();  // the last item's copy-outs read this CTA's shared memory
     if (!ok && tid == 0) {
         set_status(a.status, KDA_DEV_TIMEOUT);
         bulk_wait_all();                          // copies that still read this CTA's shared memory
@@ -1168,7 +1197,7 @@ namespace tc {
 constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand of U^T = S^T (-W)^T, O^T = S^T Q+^T
 constexpr uint32_t S_OPS = 32768;     // one chunk's workspace block (Qk, -W, Q+, Ktil^T, gl, U'), WS_BLOCK bytes
 constexpr uint32_t S_UT32 = 148480;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil, O^T += U^T Qk^T
-constexpr uint32_t S_OST = 181248;    // O staging fp32 [64 r][OST] (row stride 132: 16-byte rows, conflict-free)
+constexpr uint32_t S_OST = 181248;    // O staging fp32 [64 r][OST] of the output warps (row stride 132: conflict-free)
 constexpr int OST = 132;
 constexpr uint32_t S_NW = 215040;     // RMSNorm weight [128]
 constexpr uint32_t S_GLN = 215552;    // exp(G_last) of the next chunk [128]
@@ -1176,12 +1205,14 @@ constexpr uint32_t S_MISC = 216064;   // barriers, tensor-memory address
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
 static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0, "state smem layout");
 static_assert(S_UT32 + D * CH * 4 <= S_OST && S_OST + CH * OST * 4 <= S_NW, "state smem layout");
-constexpr int NTS = 384;              // warps 0-7: the state chain; warps 8-11: the output epilogue
+constexpr int NCW = 8;                // chain warps: two per tensor-memory lane quadrant
+constexpr int NTS = 32 * NCW + 128;   // and four output warps
+static_assert(NCW * 32 == 256, "the named barriers below count 256 chain threads");
 
-// TMEM columns: S^T [0,128), U^T [128,192), O^T [192,256)
-constexpr uint32_t T_S = 0, T_U = 128, T_O = 192;
+// TMEM columns: S^T [0,128), U^T [128,192), O^T in two buffers [192,256) and [256,320)
+constexpr uint32_t T_S = 0, T_U = 128, T_O = 192, T_COLS = 512;
 
-// Barrier 1 over the 256 threads of the state warps (the output warps run their own loop).
+// Barrier 1 over the 256 chain threads, barrier 2 over the 128 output threads (each group runs its own loop).
 __device__ __forceinline__ void state_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ bool state_sync_or(bool p) {
     uint32_t r;
@@ -1192,17 +1223,28 @@ __device__ __forceinline__ bool state_sync_or(bool p) {
         : "memory");
     return r != 0;
 }
+__device__ __forceinline__ bool out_sync_or(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 2, 128, pi;\n selp.u32 %0, 1, 0, po;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)p)
+        : "memory");
+    return r != 0;
+}
 
-// The sequential chunk pass of one (sequence, head).  The state warps run the recurrence with S^T in tensor
+// The sequential chunk pass of one (sequence, head).  The chain warps run the recurrence with S^T in tensor
 // memory, kept decayed by the NEXT chunk's exp(G_last) so that the chunk update is one accumulating MMA:
-//   U^T  = S^T (-W)^T                 (MMA, no accumulate)      O^T  = S^T Q+^T
+//   U^T  = S^T (-W)^T                 (MMA, no accumulate)
 //   U    = U' + U^T read back         -> tf32 operand tile
-//   O^T += U^T Qk^T                   S^T += U^T Ktil           (MMAs; S^T already holds S^T diag(exp(G_last)))
+//   S^T += U^T Ktil                   (MMA; S^T already holds S^T diag(exp(G_last)))
 //   S pass: bf16 operand tile of the new S, checkpoint, then S^T diag(exp(G_last of the next chunk)) back to
 //   tensor memory (or the final state to dst).
-// The O tile goes through a staging buffer to the output warps, which apply the gated RMSNorm and store y
-// while the state warps go on with the next chunk.  The chunk block arrives in three bulk copies, each issued
-// as soon as the previous chunk no longer reads its region.
+// The output MMAs O^T = S^T Q+^T + U^T Qk^T go to one of two tensor-memory buffers, which the output warps read
+// themselves: they apply the gated RMSNorm and store y while the chain goes on, and release the buffer for the
+// chunk after next.  Each chain warp owns one lane quadrant (32 value channels) and half of the columns:
+// 64 key channels of S, 32 tokens of U.  The chunk block arrives in three bulk copies, each issued as soon as
+// the previous chunk no longer reads its region.
 __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillArgs a, const Layout2 L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1220,10 +1262,9 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     uint64_t *bar_w = reinterpret_cast<uint64_t *>(sm + S_MISC);  // -W and Q+ of a chunk
     uint64_t *bar_u = bar_w + 1;                                    // U'
     uint64_t *bar_b = bar_w + 2;                                    // Qk and Ktil^T (+ exp(G_last))
-    uint64_t *bar_mma = bar_w + 3;
-    uint64_t *bar_full = bar_w + 4;   // O staged: one arrival per state warp
-    uint64_t *bar_empty = bar_w + 5;  // O consumed: one arrival per output warp
-    uint64_t *bar_o = bar_w + 6;      // the O^T MMAs of a chunk
+    uint64_t *bar_mma = bar_w + 3;                                  // the U^T and the S^T MMAs
+    uint64_t *bar_o = bar_w + 4;      // [2] the O^T MMAs of a chunk into buffer b
+    uint64_t *bar_ofree = bar_w + 6;  // [2] buffer b read by the output warps (one arrival per warp)
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
     const int64_t start = a.start_pos[n];
     const int32_t c0 = wsp<int32_t>(a, L.off_seqc)[n], c1 = wsp<int32_t>(a, L.off_seqc)[n + 1];
@@ -1241,7 +1282,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     const uint8_t *blk0 = reinterpret_cast<const uint8_t *>(a.ws) + L.off_blk;
     auto blk_of = [&](int32_t c) { return blk0 + ((size_t)c * H + h) * WS_BLOCK; };
     // -W and Q+ complete one phase of bar_w together: -W is copied as soon as the U^T MMAs are done with
-    // it, Q+ once every MMA of the chunk is (the O^T MMAs that read it are issued after the U^T commit)
+    // it, Q+ once every MMA of the chunk before the S^T commit is (the O^T MMAs that read it precede it)
     auto issue_w = [&](int32_t c) {
         mbar_arrive_expect_tx(bar_w, 2 * CH * D * 2);
         bulk_g2s(ops + WS_W, blk_of(c) + WS_W, CH * D * 2, bar_w);
@@ -1261,13 +1302,14 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     // that completes each (read only on the exit after a timed-out wait)
     bool out_w = false, out_u = false, out_b = false;
     uint32_t par_w = 0, par_u = 0, par_b = 0;
-    if (warp == 0) umma::alloc(tmem_s, 256);
+    if (warp == 0) umma::alloc(tmem_s, T_COLS);
     for (int jj = tid; jj < D; jj += NTS) nw[jj] = __ldg(a.norm_w + jj);
     if (tid == 0) {
         for (int b = 0; b < 4; ++b) mbar_init(bar_w + b, 1);
-        mbar_init(bar_o, 1);
-        mbar_init(bar_full, 8);
-        mbar_init(bar_empty, 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_o + b, 1);
+            mbar_init(bar_ofree + b, 4);
+        }
         fence_mbar_init();
         if (!empty) {
             issue_w(cb);
@@ -1282,41 +1324,43 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     umma::fence_after();
     const uint32_t tmem = *tmem_s;
 
-    if (warp < 8) {
-        // ================================ state warps ================================
-        const int quad = warp & 3, half = warp >> 2;
+    if (warp < NCW) {
+        // ================================ chain warps ================================
+        const int quad = warp & 3, part = warp >> 2;
         const int j = 32 * quad + lane;  // this thread's value channel = tensor-memory lane
         const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+        const int i0 = 64 * part;        // this thread's key channels of S: i0 .. i0 + 63
+        const int r0 = 32 * part;        // this thread's tokens of U: r0 .. r0 + 31
         // initial state: its bf16 operand tile, and S^T diag(exp(G_last of the first chunk)) in tensor memory
         {
             const float *gl0 = !empty ? reinterpret_cast<const float *>(blk_of(cb) + WS_GL) : nullptr;
             float v[32];
-            for (int part = 0; part < 2; ++part) {
-                const int i0 = 64 * half + 32 * part;
+            for (int g = 0; g < 2; ++g) {
+                const int ig = i0 + 32 * g;
                 if (first) {
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
-                        v[t] = src >= 0 ? load_state(a.S, a.state_bf16, (((size_t)src * H + h) * D + i0 + t) * D + j)
+                        v[t] = src >= 0 ? load_state(a.S, a.state_bf16, (((size_t)src * H + h) * D + ig + t) * D + j)
                                         : 0.f;
                 } else {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] = carry[(size_t)(i0 + t) * D + j];
+                    for (int t = 0; t < 32; ++t) v[t] = carry[(size_t)(ig + t) * D + j];
                 }
-                if (empty) {  // empty sequence: the state and window pass through unchanged
+                if (empty) {  // empty sequence: the state passes through unchanged
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
-                        store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
+                        store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + ig + t) * D + j, v[t]);
                     continue;
                 }
 #pragma unroll
-                for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
+                for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, ig + t, v + t);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] *= __ldg(gl0 + i0 + t);
-                umma::st32(tmem + lane_off + T_S + i0, v);
+                for (int t = 0; t < 32; ++t) v[t] *= __ldg(gl0 + ig + t);
+                umma::st32(tmem + lane_off + T_S + ig, v);
             }
-            if (empty) {
+            if (empty) {  // and so does the window
                 uint16_t *cw = a.conv + ((size_t)dst * H + h) * (kConvW - 1) * CC;
-                for (int idx = tid; idx < (kConvW - 1) * CC; idx += 256)
+                for (int idx = tid; idx < (kConvW - 1) * CC; idx += 32 * NCW)
                     cw[idx] = src >= 0 ? a.conv[((size_t)src * H + h) * (kConvW - 1) * CC + idx] : (uint16_t)0;
             }
         }
@@ -1324,8 +1368,8 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         umma::fence_before();
         state_sync();
         umma::fence_after();
-        uint32_t ph_w = 0, ph_u = 0, ph_b = 0, ph_m = 0, ph_o = 0;
-        bool ok = true;
+        uint32_t ph_w = 0, ph_u = 0, ph_b = 0, ph_m = 0;
+        bool ok = true, t0ok = true;  // t0ok: thread 0's waits on the output warps' buffer releases
         // checkpoint boundaries: a running next boundary, its slot fetched one boundary ahead (no division in
         // the loop); chunk entries are fetched one chunk ahead
         // (the boundaries at or before this launch's first position belong to the chunks before it)
@@ -1340,6 +1384,8 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         int64_t p_nx = pb;
         for (int32_t c = cb; c < ce; ++c) {
             const ChunkEnt e = e_nx;
+            const int ob = (c - cb) & 1;                        // O^T buffer of this chunk
+            const uint32_t opar = (uint32_t)((c - cb) >> 1) & 1u;  // parity of this use of it
             const int64_t pend = p_nx + e.n;
             const bool has_next = c + 1 < ce;
             if (has_next) {
@@ -1355,16 +1401,22 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             }
             const float gnext = (tid < D && has_next) ? __ldg(reinterpret_cast<const float *>(blk_of(c + 1) + WS_GL) + tid)
                                                       : 1.f;
-            // ---- U^T = S^T (-W)^T and O^T = S^T Q+^T (if -W / Q+ never arrive, nothing is committed and
-            //      every thread's bounded wait on bar_mma gives up) ----
+            // ---- U^T = S^T (-W)^T; then, once the output warps have read this O^T buffer (two chunks ago),
+            //      O^T = S^T Q+^T.  If -W / Q+ never arrive, nothing is committed and every thread's bounded wait
+            //      on bar_mma gives up ----
             if (tid == 0 && mbar_wait(bar_w, ph_w)) {
                 out_w = false;
                 const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
                 for (int ks = 0; ks < D / 16; ++ks)
                     umma::mma_bf16(tmem + T_U, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_W, CH, ks), idp, ks > 0);
                 umma::commit(bar_mma);  // U^T is read back first; the O^T MMAs complete meanwhile
-                for (int ks = 0; ks < D / 16; ++ks)
-                    umma::mma_bf16(tmem + T_O, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_QP, CH, ks), idp, ks > 0);
+                if (c - cb >= 2 && !mbar_wait(bar_ofree + ob, opar ^ 1u)) t0ok = false;
+                umma::fence_after();
+                if (t0ok) {
+                    const uint32_t tob = tmem + T_O + 64u * (uint32_t)ob;
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma::mma_bf16(tob, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_QP, CH, ks), idp, ks > 0);
+                }
             }
             ph_w ^= 1;
             // each thread waits for U^T itself; a timed-out wait is voted on at the barrier after the U tiles
@@ -1376,7 +1428,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 out_w = true;
                 par_w = ph_w;
             }
-            // ---- U = U' + U^T -> its tf32 operand tile ----
+            // ---- U = U' + U^T -> its tf32 operand tile (this thread: tokens r0 .. r0 + 31) ----
             const bool oku = mbar_wait(bar_u, ph_u);
             if (oku) out_u = false;
             ok = __all_sync(0xffffffffu, oku && ok);  // warp-uniform: the load is a warp operation
@@ -1385,23 +1437,23 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 const float *up = reinterpret_cast<const float *>(ops + WS_UP);
                 float v[32];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] = up[(32 * half + t) * D + j];  // in flight with the U^T load
+                for (int t = 0; t < 32; ++t) v[t] = up[(r0 + t) * D + j];  // in flight with the U^T load
                 uint32_t r[32];
-                umma::ld32_issue(tmem + lane_off + T_U + 32 * half, r);
+                umma::ld32_issue(tmem + lane_off + T_U + r0, r);
                 umma::wait_ld(r);
 #pragma unroll
                 for (int t = 0; t < 32; ++t) v[t] += __uint_as_float(r[t]);
 #pragma unroll
                 for (int t = 0; t < 32; t += 4)
-                    umma::st_tf32x4(Ut32, D, j, 32 * half + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
+                    umma::st_tf32x4(Ut32, D, j, r0 + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
             }
             if (tid < D) gln[tid] = gnext;
             fence_proxy_async_smem();
             umma::fence_before();
-            ok = !state_sync_or(!ok);
+            ok = !state_sync_or(!(ok && t0ok));
             umma::fence_after();
             if (!ok) break;
-            // ---- O^T += U^T Qk^T and S^T += U^T Ktil ----
+            // ---- S^T += U^T Ktil, then O^T += U^T Qk^T ----
             if (tid == 0) {
                 if (has_next) {  // U' has been read by every thread
                     issue_u(c + 1);
@@ -1417,10 +1469,10 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                                        true);
                     umma::commit(bar_mma);  // the S pass needs only S^T
                     const uint32_t ido = umma::idesc(umma::kTF32, 128, CH);
+                    const uint32_t tob = tmem + T_O + 64u * (uint32_t)ob;
                     for (int ks = 0; ks < CH / 8; ++ks)
-                        umma::mma_tf32(tmem + T_O, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_QK, CH, ks), ido,
-                                       true);
-                    umma::commit(bar_o);    // covers both rounds of O^T MMAs
+                        umma::mma_tf32(tob, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_QK, CH, ks), ido, true);
+                    umma::commit(bar_o + ob);  // covers both rounds of O^T MMAs: the output warps take it from here
                 }
             }
             ph_b ^= 1;
@@ -1429,64 +1481,57 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             ph_m ^= 1;
             umma::fence_after();
             if (tid == 0 && ok && has_next) issue_qp(c + 1);  // every MMA before the S^T commit is done: Q+ is free
-            // ---- S pass: bf16 tile of the new state, checkpoint, then decay by the next chunk (or the final
-            //      store); both halves of this thread's columns are loaded at once and stored back together ----
+            // ---- S pass (this thread: key channels i0 .. i0 + 63): bf16 tile of the new state, checkpoint, then
+            //      decay by the next chunk (or the final store); both groups of 32 are loaded at once and stored
+            //      back together ----
             if (ok) {
                 uint32_t ra[32], rb[32];
-                const int ia = 64 * half, ib = ia + 32;
-                umma::ld32_issue(tmem + lane_off + T_S + ia, ra);
-                umma::ld32_issue(tmem + lane_off + T_S + ib, rb);
+                umma::ld32_issue(tmem + lane_off + T_S + i0, ra);
+                umma::ld32_issue(tmem + lane_off + T_S + i0 + 32, rb);
                 umma::wait_ld(ra);
                 umma::wait_ld(rb);
-                auto s_part = [&](uint32_t *r, int i0) {
+                auto s_part = [&](uint32_t *r, int ig) {
                     float v[32];
 #pragma unroll
                     for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
                     if (ck >= 0) {
 #pragma unroll
                         for (int t = 0; t < 32; ++t)
-                            store_state(a.S, a.state_bf16, (((size_t)ck * H + h) * D + i0 + t) * D + j, v[t]);
+                            store_state(a.S, a.state_bf16, (((size_t)ck * H + h) * D + ig + t) * D + j, v[t]);
                     }
                     if (has_next) {
 #pragma unroll
-                        for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + t, v + t);
+                        for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, ig + t, v + t);
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) v[t] *= gln[i0 + t];
-                        umma::st32_issue(tmem + lane_off + T_S + i0, v);
+                        for (int t = 0; t < 32; ++t) v[t] *= gln[ig + t];
+                        umma::st32_issue(tmem + lane_off + T_S + ig, v);
                     } else if (last) {
 #pragma unroll
                         for (int t = 0; t < 32; ++t)
-                            store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + i0 + t) * D + j, v[t]);
+                            store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + ig + t) * D + j, v[t]);
                     } else {
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) carry[(size_t)(i0 + t) * D + j] = v[t];
+                        for (int t = 0; t < 32; ++t) carry[(size_t)(ig + t) * D + j] = v[t];
                     }
                 };
-                s_part(ra, ia);
-                s_part(rb, ib);
+                s_part(ra, i0);
+                s_part(rb, i0 + 32);
                 umma::wait_st();
             }
-            // ---- O^T -> the staging buffer of the output warps (once they have consumed the previous one) ----
-            if (c > cb) ok = __all_sync(0xffffffffu, mbar_wait(bar_empty, (uint32_t)(c - cb - 1) & 1u) && ok);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_o, ph_o) && ok);
-            ph_o ^= 1;
-            umma::fence_after();
-            if (tid == 0 && ok && has_next) {  // every MMA of this chunk is done: Qk, Ktil^T free
-                issue_b(c + 1);
-                out_b = true;
-                par_b = ph_b;
+            // Qk and Ktil^T of the next chunk, once the O^T MMAs that read Qk are done (thread 0; the S^T MMAs
+            // that read Ktil^T are)
+            if (tid == 0 && ok && has_next) {
+                if (mbar_wait(bar_o + ob, opar)) {
+                    issue_b(c + 1);
+                    out_b = true;
+                    par_b = ph_b;
+                } else {
+                    t0ok = false;
+                }
             }
-            if (ok) {
-                float v[32];
-                umma::ld32(tmem + lane_off + T_O + 32 * half, v);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) Ost[(32 * half + t) * OST + j] = v[t];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(bar_full, 0);
             fence_proxy_async_smem();
             umma::fence_before();
-            ok = !state_sync_or(!ok);
+            ok = !state_sync_or(!(ok && t0ok));
             umma::fence_after();
             if (!ok) break;
         }
@@ -1501,7 +1546,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         }
     } else {
         // ================================ output warps ================================
-        const int ow = warp - 8;  // tokens ow, ow + 4, ..., one warp per token, 4 contiguous channels per lane
+        const int ow = warp - NCW;  // its lane quadrant (NCW % 4 == 0); tokens ow, ow + 4, ..., one warp per token
         uint2 zr[16];
         auto fetch_gates = [&](int32_t c) {  // the output gate of this warp's tokens of chunk c
             const ChunkEnt e = ent[c];
@@ -1516,45 +1561,66 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         if (!empty) fetch_gates(cb);
         for (int32_t c = cb; c < ce; ++c) {
             const ChunkEnt e = ent[c];
-            if (!mbar_wait(bar_full, (uint32_t)(c - cb) & 1u)) {
-                if (lane == 0) set_status(a.status, KDA_DEV_TIMEOUT);
+            const int ob = (c - cb) & 1;
+            const uint32_t opar = (uint32_t)((c - cb) >> 1) & 1u;
+            // O^T of this chunk from its tensor-memory buffer (this warp: value channels 32 ow .. 32 ow + 31)
+            const bool okw = __all_sync(0xffffffffu, mbar_wait(bar_o + ob, opar));
+            if (out_sync_or(!okw)) {  // every output warp before the staging is rewritten; a timeout ends them all
+                if (tid == 32 * NCW) set_status(a.status, KDA_DEV_TIMEOUT);
                 break;
             }
-            const float4 w4 = *reinterpret_cast<const float4 *>(nw + 4 * lane);
-            // all 16 rows are read before any y store (the stores could otherwise be taken to alias the
-            // staging), and their reductions are interleaved
-            float4 o16[16];
-            float ss[16];
+            umma::fence_after();
+            const uint32_t tob = tmem + ((uint32_t)(32 * ow) << 16) + T_O + 64u * (uint32_t)ob;
+            const int jo = 32 * ow + lane;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                o16[k] = *reinterpret_cast<const float4 *>(Ost + (ow + 4 * k) * OST + 4 * lane);
-                ss[k] = o16[k].x * o16[k].x;
-                ss[k] = fmaf(o16[k].y, o16[k].y, ss[k]);
-                ss[k] = fmaf(o16[k].z, o16[k].z, ss[k]);
-                ss[k] = fmaf(o16[k].w, o16[k].w, ss[k]);
+            for (int hf = 0; hf < 2; ++hf) {  // tokens 32 hf .. 32 hf + 31
+                uint32_t va[32];
+                umma::ld32_issue(tob + 32 * hf, va);
+                umma::wait_ld(va);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) Ost[(32 * hf + t) * OST + jo] = __uint_as_float(va[t]);
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int k = 0; k < 16; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], o);
+            umma::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(bar_empty, 0);  // the staging has been read
+            if (lane == 0) mbar_arrive_expect_tx(bar_ofree + ob, 0);  // this quadrant of the buffer is read
+            out_sync_or(false);  // the whole O tile is staged
+            const float4 w4 = *reinterpret_cast<const float4 *>(nw + 4 * lane);
+            // tokens in two groups of 8: each group's rows are read before any of its y stores (the stores could
+            // otherwise be taken to alias the staging), and their reductions are interleaved
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int r = ow + 4 * k;
-                const float4 o4 = o16[k];
-                const float rr = rsqrtf(ss[k] * (1.0f / D) + a.rms_eps);
-                if (r < e.n) {
-                    float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
-                    if (a.z) {
-                        y0 *= sigmoid_gate(bf2f((uint16_t)(zr[k].x & 0xffff)));
-                        y1 *= sigmoid_gate(bf2f((uint16_t)(zr[k].x >> 16)));
-                        y2 *= sigmoid_gate(bf2f((uint16_t)(zr[k].y & 0xffff)));
-                        y3 *= sigmoid_gate(bf2f((uint16_t)(zr[k].y >> 16)));
+            for (int g = 0; g < 2; ++g) {
+                float4 o8[8];
+                float ss[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    o8[k] = *reinterpret_cast<const float4 *>(Ost + (ow + 4 * (8 * g + k)) * OST + 4 * lane);
+                    ss[k] = o8[k].x * o8[k].x;
+                    ss[k] = fmaf(o8[k].y, o8[k].y, ss[k]);
+                    ss[k] = fmaf(o8[k].z, o8[k].z, ss[k]);
+                    ss[k] = fmaf(o8[k].w, o8[k].w, ss[k]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], o);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int r = ow + 4 * (8 * g + k);
+                    const float4 o4 = o8[k];
+                    const float rr = rsqrtf(ss[k] * (1.0f / D) + a.rms_eps);
+                    if (r < e.n) {
+                        float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
+                        if (a.z) {
+                            const uint2 zz = zr[8 * g + k];
+                            y0 *= sigmoid_gate(bf2f((uint16_t)(zz.x & 0xffff)));
+                            y1 *= sigmoid_gate(bf2f((uint16_t)(zz.x >> 16)));
+                            y2 *= sigmoid_gate(bf2f((uint16_t)(zz.y & 0xffff)));
+                            y3 *= sigmoid_gate(bf2f((uint16_t)(zz.y >> 16)));
+                        }
+                        *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
+                            make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
+                                       (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
                     }
-                    *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
-                        make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
-                                   (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
                 }
             }
             if (c + 1 < ce) fetch_gates(c + 1);
@@ -1562,7 +1628,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     }
     umma::fence_before();
     __syncthreads();
-    if (warp == 0) umma::dealloc(tmem, 256);
+    if (warp == 0) umma::dealloc(tmem, T_COLS);
 }
 
 }  // namespace tc
