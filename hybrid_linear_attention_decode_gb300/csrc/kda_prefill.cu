@@ -1206,13 +1206,14 @@ constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
 static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0, "state smem layout");
 static_assert(S_UT32 + D * CH * 4 <= S_OST && S_OST + CH * OST * 4 <= S_NW, "state smem layout");
 constexpr int NCW = 8;                // chain warps: two per tensor-memory lane quadrant
-constexpr int NTS = 32 * NCW + 128;   // and four output warps
-static_assert(NCW * 32 == 256, "the named barriers below count 256 chain threads");
+constexpr int NOW = 8;                // output warps: two per lane quadrant
+constexpr int NTS = 32 * (NCW + NOW);
+static_assert(NCW * 32 == 256 && NOW * 32 == 256, "the named barriers below count 256 threads each");
 
 // TMEM columns: S^T [0,128), U^T [128,192), O^T in two buffers [192,256) and [256,320)
 constexpr uint32_t T_S = 0, T_U = 128, T_O = 192, T_COLS = 512;
 
-// Barrier 1 over the 256 chain threads, barrier 2 over the 128 output threads (each group runs its own loop).
+// Barrier 1 over the 256 chain threads, barrier 2 over the 256 output threads (each group runs its own loop).
 __device__ __forceinline__ void state_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ bool state_sync_or(bool p) {
     uint32_t r;
@@ -1226,7 +1227,7 @@ __device__ __forceinline__ bool state_sync_or(bool p) {
 __device__ __forceinline__ bool out_sync_or(bool p) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 2, 128, pi;\n selp.u32 %0, 1, 0, po;\n}"
+        "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 2, 256, pi;\n selp.u32 %0, 1, 0, po;\n}"
         : "=r"(r)
         : "r"((uint32_t)p)
         : "memory");
@@ -1240,9 +1241,9 @@ __device__ __forceinline__ bool out_sync_or(bool p) {
 //   S^T += U^T Ktil                   (MMA; S^T already holds S^T diag(exp(G_last)))
 //   S pass: bf16 operand tile of the new S, checkpoint, then S^T diag(exp(G_last of the next chunk)) back to
 //   tensor memory (or the final state to dst).
-// The output MMAs O^T = S^T Q+^T + U^T Qk^T go to one of two tensor-memory buffers, which the output warps read
-// themselves: they apply the gated RMSNorm and store y while the chain goes on, and release the buffer for the
-// chunk after next.  Each chain warp owns one lane quadrant (32 value channels) and half of the columns:
+// The output MMAs O^T = S^T Q+^T + U^T Qk^T go to one of two tensor-memory buffers, which the eight output warps
+// read themselves: they apply the gated RMSNorm and store y while the chain goes on, and release the buffer for
+// the chunk after next.  Each chain warp owns one lane quadrant (32 value channels) and half of the columns:
 // 64 key channels of S, 32 tokens of U.  The chunk block arrives in three bulk copies, each issued as soon as
 // the previous chunk no longer reads its region.
 __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillArgs a, const Layout2 L) {
@@ -1264,7 +1265,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     uint64_t *bar_b = bar_w + 2;                                    // Qk and Ktil^T (+ exp(G_last))
     uint64_t *bar_mma = bar_w + 3;                                  // the U^T and the S^T MMAs
     uint64_t *bar_o = bar_w + 4;      // [2] the O^T MMAs of a chunk into buffer b
-    uint64_t *bar_ofree = bar_w + 6;  // [2] buffer b read by the output warps (one arrival per warp)
+    uint64_t *bar_ofree = bar_w + 6;  // [2] buffer b read by the output warps (one arrival per output warp)
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
     const int64_t start = a.start_pos[n];
     const int32_t c0 = wsp<int32_t>(a, L.off_seqc)[n], c1 = wsp<int32_t>(a, L.off_seqc)[n + 1];
@@ -1308,7 +1309,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         for (int b = 0; b < 4; ++b) mbar_init(bar_w + b, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_o + b, 1);
-            mbar_init(bar_ofree + b, 4);
+            mbar_init(bar_ofree + b, NOW);
         }
         fence_mbar_init();
         if (!empty) {
@@ -1481,16 +1482,13 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             ph_m ^= 1;
             umma::fence_after();
             if (tid == 0 && ok && has_next) issue_qp(c + 1);  // every MMA before the S^T commit is done: Q+ is free
-            // ---- S pass (this thread: key channels i0 .. i0 + 63): bf16 tile of the new state, checkpoint, then
-            //      decay by the next chunk (or the final store); both groups of 32 are loaded at once and stored
-            //      back together ----
+            // ---- S pass (this thread: key channels i0 .. i0 + 63, in two groups of 32): bf16 tile of the new
+            //      state, checkpoint, then decay by the next chunk (or the final store) ----
             if (ok) {
-                uint32_t ra[32], rb[32];
-                umma::ld32_issue(tmem + lane_off + T_S + i0, ra);
-                umma::ld32_issue(tmem + lane_off + T_S + i0 + 32, rb);
-                umma::wait_ld(ra);
-                umma::wait_ld(rb);
-                auto s_part = [&](uint32_t *r, int ig) {
+                auto s_part = [&](int ig) {
+                    uint32_t r[32];
+                    umma::ld32_issue(tmem + lane_off + T_S + ig, r);
+                    umma::wait_ld(r);
                     float v[32];
 #pragma unroll
                     for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
@@ -1514,8 +1512,8 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                         for (int t = 0; t < 32; ++t) carry[(size_t)(ig + t) * D + j] = v[t];
                     }
                 };
-                s_part(ra, i0);
-                s_part(rb, i0 + 32);
+                s_part(i0);
+                s_part(i0 + 32);
                 umma::wait_st();
             }
             // Qk and Ktil^T of the next chunk, once the O^T MMAs that read Qk are done (thread 0; the S^T MMAs
@@ -1546,84 +1544,83 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         }
     } else {
         // ================================ output warps ================================
-        const int ow = warp - NCW;  // its lane quadrant (NCW % 4 == 0); tokens ow, ow + 4, ..., one warp per token
-        uint2 zr[16];
-        auto fetch_gates = [&](int32_t c) {  // the output gate of this warp's tokens of chunk c
-            const ChunkEnt e = ent[c];
+        // warp ow: lane quadrant ow % 4 (NCW % 4 == 0) and token half ow / 4 of the O^T buffer when staging;
+        // tokens ow, ow + 8, ..., one warp per token, for the gated RMSNorm
+        const int ow = warp - NCW, oq = ow & 3, oh = ow >> 2;
+        uint2 zr[8];
+        auto fetch_gates = [&](const ChunkEnt &e) {  // the output gate of this warp's tokens of a chunk
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int r = ow + 4 * k;
+            for (int k = 0; k < 8; ++k) {
+                const int r = ow + 8 * k;
                 zr[k] = (a.z && r < e.n)
                             ? __ldg(reinterpret_cast<const uint2 *>(a.z + ((size_t)(e.t0 + r) * H + h) * D) + lane)
                             : make_uint2(0u, 0u);
             }
         };
-        if (!empty) fetch_gates(cb);
+        ChunkEnt e_nx = !empty ? ent[cb] : ChunkEnt{};
+        if (!empty) fetch_gates(e_nx);
         for (int32_t c = cb; c < ce; ++c) {
-            const ChunkEnt e = ent[c];
+            const ChunkEnt e = e_nx;
+            if (c + 1 < ce) e_nx = ent[c + 1];  // in flight while this chunk is processed
             const int ob = (c - cb) & 1;
             const uint32_t opar = (uint32_t)((c - cb) >> 1) & 1u;
-            // O^T of this chunk from its tensor-memory buffer (this warp: value channels 32 ow .. 32 ow + 31)
+            // O^T of this chunk from its tensor-memory buffer (this warp: value channels 32 oq .. 32 oq + 31,
+            // tokens 32 oh .. 32 oh + 31)
             const bool okw = __all_sync(0xffffffffu, mbar_wait(bar_o + ob, opar));
             if (out_sync_or(!okw)) {  // every output warp before the staging is rewritten; a timeout ends them all
                 if (tid == 32 * NCW) set_status(a.status, KDA_DEV_TIMEOUT);
                 break;
             }
             umma::fence_after();
-            const uint32_t tob = tmem + ((uint32_t)(32 * ow) << 16) + T_O + 64u * (uint32_t)ob;
-            const int jo = 32 * ow + lane;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {  // tokens 32 hf .. 32 hf + 31
+            {
                 uint32_t va[32];
-                umma::ld32_issue(tob + 32 * hf, va);
+                umma::ld32_issue(tmem + ((uint32_t)(32 * oq) << 16) + T_O + 64u * (uint32_t)ob + 32u * (uint32_t)oh, va);
                 umma::wait_ld(va);
+                const int jo = 32 * oq + lane;
 #pragma unroll
-                for (int t = 0; t < 32; ++t) Ost[(32 * hf + t) * OST + jo] = __uint_as_float(va[t]);
+                for (int t = 0; t < 32; ++t) Ost[(32 * oh + t) * OST + jo] = __uint_as_float(va[t]);
             }
             umma::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(bar_ofree + ob, 0);  // this quadrant of the buffer is read
+            if (lane == 0) mbar_arrive_expect_tx(bar_ofree + ob, 0);  // this warp's part of the buffer is read
             out_sync_or(false);  // the whole O tile is staged
             const float4 w4 = *reinterpret_cast<const float4 *>(nw + 4 * lane);
-            // tokens in two groups of 8: each group's rows are read before any of its y stores (the stores could
-            // otherwise be taken to alias the staging), and their reductions are interleaved
+            // the 8 rows are read before any y store (the stores could otherwise be taken to alias the staging),
+            // and their reductions are interleaved
+            float4 o8[8];
+            float ss[8];
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                float4 o8[8];
-                float ss[8];
+            for (int k = 0; k < 8; ++k) {
+                o8[k] = *reinterpret_cast<const float4 *>(Ost + (ow + 8 * k) * OST + 4 * lane);
+                ss[k] = o8[k].x * o8[k].x;
+                ss[k] = fmaf(o8[k].y, o8[k].y, ss[k]);
+                ss[k] = fmaf(o8[k].z, o8[k].z, ss[k]);
+                ss[k] = fmaf(o8[k].w, o8[k].w, ss[k]);
+            }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    o8[k] = *reinterpret_cast<const float4 *>(Ost + (ow + 4 * (8 * g + k)) * OST + 4 * lane);
-                    ss[k] = o8[k].x * o8[k].x;
-                    ss[k] = fmaf(o8[k].y, o8[k].y, ss[k]);
-                    ss[k] = fmaf(o8[k].z, o8[k].z, ss[k]);
-                    ss[k] = fmaf(o8[k].w, o8[k].w, ss[k]);
-                }
+            for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
+                for (int k = 0; k < 8; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], o);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], o);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int r = ow + 4 * (8 * g + k);
-                    const float4 o4 = o8[k];
-                    const float rr = rsqrtf(ss[k] * (1.0f / D) + a.rms_eps);
-                    if (r < e.n) {
-                        float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
-                        if (a.z) {
-                            const uint2 zz = zr[8 * g + k];
-                            y0 *= sigmoid_gate(bf2f((uint16_t)(zz.x & 0xffff)));
-                            y1 *= sigmoid_gate(bf2f((uint16_t)(zz.x >> 16)));
-                            y2 *= sigmoid_gate(bf2f((uint16_t)(zz.y & 0xffff)));
-                            y3 *= sigmoid_gate(bf2f((uint16_t)(zz.y >> 16)));
-                        }
-                        *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
-                            make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
-                                       (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
+            for (int k = 0; k < 8; ++k) {
+                const int r = ow + 8 * k;
+                const float4 o4 = o8[k];
+                const float rr = rsqrtf(ss[k] * (1.0f / D) + a.rms_eps);
+                if (r < e.n) {
+                    float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
+                    if (a.z) {
+                        const uint2 zz = zr[k];
+                        y0 *= sigmoid_gate(bf2f((uint16_t)(zz.x & 0xffff)));
+                        y1 *= sigmoid_gate(bf2f((uint16_t)(zz.x >> 16)));
+                        y2 *= sigmoid_gate(bf2f((uint16_t)(zz.y & 0xffff)));
+                        y3 *= sigmoid_gate(bf2f((uint16_t)(zz.y >> 16)));
                     }
+                    *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
+                        make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
+                                   (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
                 }
             }
-            if (c + 1 < ce) fetch_gates(c + 1);
+            if (c + 1 < ce) fetch_gates(e_nx);
         }
     }
     umma::fence_before();
