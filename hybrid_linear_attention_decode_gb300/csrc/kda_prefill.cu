@@ -912,8 +912,10 @@ __global__ void __launch_bounds__(NTI, 1)
             umma::fence_after();
             if (tid == 0) {
                 const uint32_t id = umma::idesc(umma::kTF32, 128, CH);
+                const uint64_t dX = umma::sdesc_k(X1, 128, 0), dM = umma::sdesc_k(Km, CH, 0);
+#pragma unroll
                 for (int ks = 0; ks < 64 / 8; ++ks)
-                    umma::mma_tf32(tmem, umma::sdesc_k(X1, 128, ks), umma::sdesc_k(Km, CH, ks), id, hh > 0 || ks > 0);
+                    umma::mma_tf32(tmem, umma::sdesc_at(dX, 128, ks), umma::sdesc_at(dM, CH, ks), id, hh > 0 || ks > 0);
                 umma::commit(bar);
             }
         };
@@ -1099,10 +1101,12 @@ __global__ void __launch_bounds__(NTI, 1)
     umma::fence_after();
     if (tid == 0) {
         const uint32_t id = umma::idesc(umma::kTF32, 128, CH);
+        const uint64_t dT = umma::sdesc_k(Tt, CH, 0), dKp = umma::sdesc_k(Kpt, D, 0), dV = umma::sdesc_k(Vt, D, 0);
+#pragma unroll
         for (int ks = 0; ks < CH / 8; ++ks) {
-            const uint64_t bt = umma::sdesc_k(Tt, CH, ks);
-            umma::mma_tf32(tmem + 64, umma::sdesc_k(Kpt, D, ks), bt, id, ks > 0);
-            umma::mma_tf32(tmem + 128, umma::sdesc_k(Vt, D, ks), bt, id, ks > 0);
+            const uint64_t bt = umma::sdesc_at(dT, CH, ks);
+            umma::mma_tf32(tmem + 64, umma::sdesc_at(dKp, D, ks), bt, id, ks > 0);
+            umma::mma_tf32(tmem + 128, umma::sdesc_at(dV, D, ks), bt, id, ks > 0);
         }
         umma::commit(bar);
     }
@@ -1408,15 +1412,19 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             if (tid == 0 && mbar_wait(bar_w, ph_w)) {
                 out_w = false;
                 const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
+                const uint64_t dS = umma::sdesc_k(Sst, D, 0), dW = umma::sdesc_k(ops + WS_W, CH, 0);
+#pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    umma::mma_bf16(tmem + T_U, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_W, CH, ks), idp, ks > 0);
+                    umma::mma_bf16(tmem + T_U, umma::sdesc_at(dS, D, ks), umma::sdesc_at(dW, CH, ks), idp, ks > 0);
                 umma::commit(bar_mma);  // U^T is read back first; the O^T MMAs complete meanwhile
                 if (c - cb >= 2 && !mbar_wait(bar_ofree + ob, opar ^ 1u)) t0ok = false;
                 umma::fence_after();
                 if (t0ok) {
                     const uint32_t tob = tmem + T_O + 64u * (uint32_t)ob;
+                    const uint64_t dQ = umma::sdesc_k(ops + WS_QP, CH, 0);
+#pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
-                        umma::mma_bf16(tob, umma::sdesc_k(Sst, D, ks), umma::sdesc_k(ops + WS_QP, CH, ks), idp, ks > 0);
+                        umma::mma_bf16(tob, umma::sdesc_at(dS, D, ks), umma::sdesc_at(dQ, CH, ks), idp, ks > 0);
                 }
             }
             ph_w ^= 1;
@@ -1465,14 +1473,17 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 if (okb) {
                     out_b = false;
                     const uint32_t ids = umma::idesc(umma::kTF32, 128, D);
+                    const uint64_t dU = umma::sdesc_k(Ut32, D, 0), dK = umma::sdesc_k(ops + WS_KT, D, 0);
+#pragma unroll
                     for (int ks = 0; ks < CH / 8; ++ks)
-                        umma::mma_tf32(tmem + T_S, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_KT, D, ks), ids,
-                                       true);
+                        umma::mma_tf32(tmem + T_S, umma::sdesc_at(dU, D, ks), umma::sdesc_at(dK, D, ks), ids, true);
                     umma::commit(bar_mma);  // the S pass needs only S^T
                     const uint32_t ido = umma::idesc(umma::kTF32, 128, CH);
                     const uint32_t tob = tmem + T_O + 64u * (uint32_t)ob;
+                    const uint64_t dQk = umma::sdesc_k(ops + WS_QK, CH, 0);
+#pragma unroll
                     for (int ks = 0; ks < CH / 8; ++ks)
-                        umma::mma_tf32(tob, umma::sdesc_k(Ut32, D, ks), umma::sdesc_k(ops + WS_QK, CH, ks), ido, true);
+                        umma::mma_tf32(tob, umma::sdesc_at(dU, D, ks), umma::sdesc_at(dQk, CH, ks), ido, true);
                     umma::commit(bar_o + ob);  // covers both rounds of O^T MMAs: the output warps take it from here
                 }
             }
@@ -1558,10 +1569,10 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             }
         };
         ChunkEnt e_nx = !empty ? ent[cb] : ChunkEnt{};
-        if (!empty) fetch_gates(e_nx);
         for (int32_t c = cb; c < ce; ++c) {
             const ChunkEnt e = e_nx;
             if (c + 1 < ce) e_nx = ent[c + 1];  // in flight while this chunk is processed
+            fetch_gates(e);  // in flight while the O^T of this chunk is awaited and staged
             const int ob = (c - cb) & 1;
             const uint32_t opar = (uint32_t)((c - cb) >> 1) & 1u;
             // O^T of this chunk from its tensor-memory buffer (this warp: value channels 32 oq .. 32 oq + 31,
@@ -1620,7 +1631,6 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                                    (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
                 }
             }
-            if (c + 1 < ce) fetch_gates(e_nx);
         }
     }
     umma::fence_before();

@@ -76,6 +76,13 @@ __device__ __forceinline__ uint64_t sdesc_k(const uint8_t *tile, int R, int ks) 
     return sdesc(a);
 }
 
+// Descriptor of K slice `ks` from the descriptor of slice 0 of the same tile: only the start-address field
+// advances (by 32 bytes within a 128-byte chunk, by R * 128 bytes across chunks).  Shared-memory addresses
+// stay below 2^18 bytes, so the 14-bit field (address / 16) never carries into the next field.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t d0, int R, int ks) {
+    return d0 + (uint64_t)((((ks >> 2) * R * 128) + (ks & 3) * 32) >> 4);
+}
+
 // Instruction descriptor: fp32 accumulate, K-major A and B, M x N; kind = 1 (bf16) or 2 (tf32).
 __device__ __forceinline__ uint32_t idesc(int fmt, int M, int N, bool negate_a = false) {
     return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | ((negate_a ? 1u : 0u) << 13) |
