@@ -658,13 +658,14 @@ def run_decode_bf16(args, kda, torch, dev, stream, prm, d, seed, hbm_peak, ws):
 LONG_T, LONG_INTERVAL, LONG_DEC_N = 131072, 32768, 256
 
 
-def run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws, prefill_only=False):
+def run_long_context(args, kda, torch, dev, stream, pool, prm, seed, hbm_peak, ws, prefill_only=False,
+                     tokens=LONG_T):
     """The long-context workload: one 131072-token prefill (H=32, d=128, chunk 64, checkpoints every 32768
     tokens) into the pool, then a batch-256 decode step in which request 0 continues that sequence from its
     final state and 255 requests use other random slots.  Token inputs are drawn on the device (seeded torch
     generator, the distributions of the other workloads); 5 GB of them would be slow to draw on the host.
     prefill_only: two prefill calls and nothing else (the profile case)."""
-    T, C, I = LONG_T, PRE_CHUNK, LONG_INTERVAL
+    T, C, I = tokens, PRE_CHUNK, LONG_INTERVAL
     ns = int(pool.S.shape[0])
     g = torch.Generator(device=dev)
     g.manual_seed(seed + 11)
@@ -882,12 +883,15 @@ def run_profile_case(args):
     elif args.profile == "project":
         r = run_project(argparse.Namespace(steps=args.steps, warmup=args.warmup), kda, torch, dev, stream, seed, 1)
         print(f"profile case project: {r}")
-    elif args.profile == "long_prefill":
+    elif args.profile in ("long_prefill", "long_prefill_small"):
+        # the small case: one 32768-token sequence (512 chunks, launched in segments like the full one, one
+        # checkpoint), for captures whose per-chunk traffic scales to the 131072-token workload
         pool = kda.StatePool.empty(16, H, DK, DV, W, device=dev)
+        T = LONG_T if args.profile == "long_prefill" else LONG_T // 4
         r = run_long_context(args, kda, torch, dev, stream, pool, prm, seed, measured_peaks()[0], 1,
-                             prefill_only=True)
+                             prefill_only=True, tokens=T)
         assert r["status"] == 0
-        print(f"profile case long_prefill: {r}")
+        print(f"profile case {args.profile}: {r}")
     else:
         pool = kda.StatePool.empty(512, H, DK, DV, W, device=dev)
         r = run_prefill(argparse.Namespace(steps=1, warmup=args.warmup), kda, torch, dev, stream, pool, prm, seed,
@@ -904,7 +908,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["decode", "decode_bf16", "decode_multi", "project", "prefill",
-                                              "long_prefill"], default=None,
+                                              "long_prefill", "long_prefill_small"], default=None,
                     help="run a small case of one kernel for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:
