@@ -1,0 +1,156 @@
+"""Why the tensor-core prefill rounds its operands the way it does, checked on the CPU.
+
+The chunked form of the gated delta rule is computed here in numpy float32, with the operands of every
+product rounded exactly as the tensor-core kernels stage them (tf32 rounded to nearest, or bf16), and compared
+with the fp64 oracle on the same inputs.  This is a model of the kernels' rounding, not of their code: it
+shares nothing with the CUDA path.  It fixes three facts the kernel design rests on:
+  * the kernels' operand mix keeps the state within 1e-3 (relative Frobenius) and the outputs within 2e-2;
+  * bf16 operands everywhere (what a plain bf16 tensor-core prefill would use) miss the state bar, and so do
+    tf32 operands truncated rather than rounded (what the tensor core reads from unconverted fp32) in the
+    products that feed the state;
+  * a Qk diagonal taken from the rounded [A; Qk] MMA misses the output bar on a sequence's first token when
+    q^ and k^ are nearly orthogonal; the fp32 diagonal the kernel forms meets it.
+"""
+import numpy as np
+import pytest
+
+import kda_inputs as ki
+import oracle
+from tests.kda_testutil import s_err, y_err
+from tests.test_prefill_precision_gpu import _silu, near_orthogonal_k
+
+D, C, W = 128, 64, 4
+
+
+def tf32(x):
+    """fp32 -> tf32, round to nearest with ties away from zero (the staging conversion of the kernels)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x1000) & 0xFFFFE000).astype(np.uint32).view(np.float32)
+
+
+def tf32_truncated(x):
+    """fp32 -> tf32 by dropping the low 13 mantissa bits."""
+    return (np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) & 0xFFFFE000).view(np.float32)
+
+
+def bf16(x):
+    return ki.bf16_round(np.asarray(x, dtype=np.float32))
+
+
+# which rounding each product's operands get: [A; Qk], T [K+ | V], -W S, Q+ S, Qk U, Ktil^T U
+KERNEL_MIX = dict(aqk=tf32, tkv=tf32, ws=bf16, qs=bf16, qku=tf32, ktu=tf32)
+ALL_BF16 = dict(aqk=bf16, tkv=bf16, ws=bf16, qs=bf16, qku=bf16, ktu=bf16)
+
+
+def conv_norm_gates(tok, wts, h, t0, t1):
+    """Per-token inputs of one head from an empty window: conv + SiLU outputs (q^, k^ L2-normalised), the
+    log decay and beta, in fp64."""
+    f = {k: ki.bf16_bits_to_f64(v)[:, h] for k, v in tok.items() if v is not None}
+    x = np.concatenate([f["q"], f["k"], f["v"]], axis=1)  # [T][3D]
+    xp = np.concatenate([np.zeros((W - 1, 3 * D)), x])
+    w = wts["conv_w"][h]  # [3D][W], tap W-1 on the current input
+    conv = sum(w[:, j] * xp[j:j + len(x)] for j in range(W))
+    conv = _silu(conv)[t0:t1]
+    q, k, v = conv[:, :D], conv[:, D:2 * D], conv[:, 2 * D:]
+    q = q / np.sqrt((q * q).sum(1, keepdims=True) + 1e-6)
+    k = k / np.sqrt((k * k).sum(1, keepdims=True) + 1e-6)
+    a = f["a"][t0:t1]
+    loga = np.minimum(a, 0) - np.log1p(np.exp(-np.abs(a)))
+    beta = 1.0 / (1.0 + np.exp(-f["b"][t0:t1]))
+    z = f["z"][t0:t1]
+    return q, k, v, loga, beta, z
+
+
+def emulate(q, k, v, loga, beta, z, norm_w, mix, fp32_diag=True, scale=1.0):
+    """The chunked recurrence of one head from a zero state, chunk by chunk in the kernels' formulation, with
+    each product's operands rounded per `mix`.  Returns the bf16-rounded outputs and the final state."""
+    f32 = np.float32
+    S = np.zeros((D, D), f32)
+    ys = []
+    for c0 in range(0, len(q), C):
+        qc, kc, vc = (x[c0:c0 + C].astype(f32) for x in (q, k, v))
+        G = np.cumsum(loga[c0:c0 + C], axis=0).astype(f32)
+        bc = beta[c0:c0 + C].astype(f32)
+        n = len(qc)
+        Gm, Gl = G[min(C // 2, n - 1)], G[n - 1]
+        e1, e2 = np.exp(G - Gm).astype(f32), np.exp(Gm - G).astype(f32)
+        r = mix["aqk"]
+        Kp, Qp, Km = r(kc * e1), r(qc * e1), r(kc * e2)
+        A = np.tril(Kp @ Km.T, -1)
+        Qk = np.tril(scale * (Qp @ Km.T))
+        if fp32_diag:
+            np.fill_diagonal(Qk, scale * (qc * kc).sum(1))
+        T = np.linalg.inv(np.eye(n, dtype=f32) + bc[:, None] * A).astype(f32) * bc[None, :]
+        r = mix["tkv"]
+        Wm = r(T) @ r(kc * np.exp(G))
+        Up = r(T) @ r(vc)
+        r = mix["ws"]
+        U = (Up + r(-Wm) @ r(S)).astype(f32)
+        r1, r2 = mix["qs"], mix["qku"]
+        O = r1(scale * qc * np.exp(G)) @ r1(S) + r2(Qk) @ r2(U)
+        r = mix["ktu"]
+        S = (np.exp(Gl)[:, None] * S + r(kc * np.exp(Gl - G)).T @ r(U)).astype(f32)
+        rr = 1.0 / np.sqrt((O.astype(np.float64) ** 2).mean(1, keepdims=True) + 1e-6)
+        y = O * rr * norm_w[None, :] / (1.0 + np.exp(-z[c0:c0 + C]))
+        ys.append(bf16(y))
+    return np.concatenate(ys), S
+
+
+def reference(tok, wts, heads, T):
+    """The fp64 oracle over one sequence of T tokens from an empty state, for the given heads."""
+    f = {k: ki.bf16_bits_to_f64(v)[:, heads] for k, v in tok.items()}
+    Hs = len(heads)
+    return oracle.forward(oracle.Cfg(H=Hs, dk=D, dv=D, W=W), [0, T], [0], f["q"], f["k"], f["v"], f["a"], f["b"],
+                          f["z"], wts["conv_w"][heads], wts["norm_w"], np.zeros((1, Hs, D, D)),
+                          np.zeros((1, Hs, W - 1, 3 * D)))
+
+
+def errors(seed, T, heads, mix, fp32_diag=True):
+    wts = ki.layer_weights(seed, max(heads) + 1, D, D)
+    tok = ki.token_inputs(seed, T, max(heads) + 1, D, D)
+    ref = reference(tok, wts, heads, T)
+    ey, es = 0.0, 0.0
+    for i, h in enumerate(heads):
+        y, S = emulate(*conv_norm_gates(tok, wts, h, 0, T), wts["norm_w"], mix, fp32_diag)
+        ey = max(ey, y_err(y, ref["y"][:, i]))
+        es = max(es, s_err(S, ref["S"][0, i]))
+    return ey, es
+
+
+@pytest.mark.parametrize("seed", [100, 103])
+def test_kernel_operand_mix_meets_both_bars(seed):
+    ey, es = errors(seed, 2048, [0, 1], KERNEL_MIX)
+    assert es <= 1e-3 and ey <= 2e-2, (es, ey)
+
+
+def test_bf16_operands_everywhere_miss_the_state_bar():
+    ey, es = errors(100, 2048, [0, 1], ALL_BF16)
+    assert es > 1e-3, es
+
+
+def test_truncated_tf32_in_the_state_products_misses_the_state_bar():
+    mix = dict(KERNEL_MIX, tkv=tf32_truncated, ktu=tf32_truncated)
+    ey, es = errors(100, 2048, [0, 1], mix)
+    assert es > 1e-3, es
+
+
+def test_fp32_qk_diagonal_is_needed_for_near_orthogonal_first_tokens():
+    """First tokens whose q^ . k^ is about 1e-4: from an empty state the output is that single dot product, which
+    the rounded MMA operands get wrong by tens of percent; the fp32 diagonal keeps it within the bar."""
+    seed, H, T = 91, 4, 64
+    wts = ki.layer_weights(seed, H, D, D)
+    tok = ki.token_inputs(seed, T, H, D, D)
+    q = ki.bf16_bits_to_f64(tok["q"])
+    k = ki.bf16_bits_to_f64(tok["k"]).copy()
+    for h in range(H):
+        kk = near_orthogonal_k(q[0, h], k[0, h], wts["conv_w"][h, :D, W - 1], wts["conv_w"][h, D:2 * D, W - 1], 1e-4)
+        assert kk is not None
+        k[0, h] = kk
+    tok["k"] = ki.f32_to_bf16_bits(k.astype(np.float32))
+    ref = reference(tok, wts, list(range(H)), T)
+    worst = {True: 0.0, False: 0.0}
+    for fp32_diag in (True, False):
+        for h in range(H):
+            y, _ = emulate(*conv_norm_gates(tok, wts, h, 0, T), wts["norm_w"], KERNEL_MIX, fp32_diag)
+            worst[fp32_diag] = max(worst[fp32_diag], y_err(y[:1], ref["y"][:1, h]))
+    assert worst[True] <= 2e-2 and worst[False] > 2e-2, worst
