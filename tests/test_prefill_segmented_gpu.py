@@ -14,6 +14,7 @@ test here is bit-exact against the same work done by calls too small to be segme
   * a bf16 state pool against the fp32 pool rounded to bf16 (outputs identical, states and checkpoints
     the bf16 rounding of the fp32 ones);
   * a call captured in a CUDA graph and replayed, against the eager call;
+  * a resume in place (src == dst) against the same resume into another slot;
 and, against the fp64 oracle, one head (so that a segmented workspace fits the no-alloc entry point's
 static scratch) with a bf16 pool resumed from a stored state, no output gate and a skipped checkpoint.
 
@@ -127,6 +128,28 @@ def test_segmented_call_equals_two_resumed_calls():
     bad = [j for j in range(nck) if not (_same(pool.S[cks[j]], pool.S[cks_b[j]])
                                          and _same(pool.conv[cks[j]], pool.conv[cks_b[j]]))]
     assert not bad, f"checkpoints differ at {bad[:8]}"
+
+
+def test_segmented_in_place_resume_equals_moved_resume():
+    """A segmented call resuming one sequence in place (src == dst, the plan the prefix index makes) gives, bit
+    for bit, what the same call gives from a copy of the source into another destination: the history rows
+    the first segment reads come from the table kernel's snapshot of the source window, not from the slot the
+    last segment overwrites."""
+    kda = _kda()
+    H, interval, T, start = 8, 4096, 33000, 4096 + 17
+    assert H * 4 <= _sms() and T // CH >= 512
+    nck = _ckpt_count(start, T, interval)
+    pool, prm = _setup(kda, H, 8 + 2 * nck, seed=91)
+    tok = _tokens(92, T, H)
+    pool.S[2].copy_(pool.S[1])
+    pool.conv[2].copy_(pool.conv[1])
+    cks_a, cks_b = list(range(8, 8 + nck)), list(range(8 + nck, 8 + 2 * nck))
+    yA = _call(kda, pool, prm, tok, 0, [T], [start], [1], [1], interval, cks_a)  # in place
+    yB = _call(kda, pool, prm, tok, 0, [T], [start], [2], [3], interval, cks_b)  # moved
+    np.testing.assert_array_equal(_bits(yA), _bits(yB))
+    assert _same(pool.S[1], pool.S[3]) and _same(pool.conv[1], pool.conv[3])
+    for a_, b_ in zip(cks_a, cks_b):
+        assert _same(pool.S[a_], pool.S[b_]) and _same(pool.conv[a_], pool.conv[b_])
 
 
 def test_segmented_call_equals_per_sequence_calls():
