@@ -708,20 +708,23 @@ __global__ void __launch_bounds__(NTI, 1)
     if (!ok) break;  // the loads stay in flight: the exit path waits for them once more
     ph_in ^= 1;
     if (tid == 0) in_flight = false;
+    if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(blogit)) : 0.f;  // read from P4 on
     {   // history rows before the sequence start: the source window as it was when the call began (the
-        // table kernel's snapshot), or zeros
+        // table kernel's snapshot), or zeros.  Only an item that has such rows needs the barrier (the condition
+        // is the same for every thread).
         const ItemMeta mt = meta[it & 1];
         const int hist_src = (int)min((int64_t)(kConvW - 1), max((int64_t)0, mt.start - mt.p0 + (kConvW - 1)));
-        const uint16_t *win = wsp<uint16_t>(a, L.off_win) + ((size_t)mt.seq * H + h) * (kConvW - 1) * CC;
-        for (int idx = tid; idx < hist_src * CC; idx += NTI) {
-            const int row = idx / CC, ch = idx - (idx / CC) * CC;
-            const int64_t p = mt.p0 - (kConvW - 1) + row;
-            raw[(ch >> 7) * RAW_PART + row * D + (ch & 127)] =
-                mt.srcv >= 0 ? win[(p - mt.start + (kConvW - 1)) * CC + ch] : (uint16_t)0;
+        if (hist_src > 0) {
+            const uint16_t *win = wsp<uint16_t>(a, L.off_win) + ((size_t)mt.seq * H + h) * (kConvW - 1) * CC;
+            for (int idx = tid; idx < hist_src * CC; idx += NTI) {
+                const int row = idx / CC, ch = idx - (idx / CC) * CC;
+                const int64_t p = mt.p0 - (kConvW - 1) + row;
+                raw[(ch >> 7) * RAW_PART + row * D + (ch & 127)] =
+                    mt.srcv >= 0 ? win[(p - mt.start + (kConvW - 1)) * CC + ch] : (uint16_t)0;
+            }
+            __syncthreads();
         }
     }
-    if (tid < CH) beta[tid] = tid < ntok ? sigmoidf_(bf2f(blogit)) : 0.f;
-    __syncthreads();
     // ---- P1: causal conv + SiLU over (channel, block of 16 rows) units, three per thread: the block's three
     //      history rows come from the staged raw rows, the window runs in registers along the block ----
 #pragma unroll 1
@@ -940,15 +943,17 @@ __global__ void __launch_bounds__(NTI, 1)
         }
     }
     // ---- P3: A (strict lower, fp32 in smem) and Qk (scaled, lower with the fp32 diagonal, tf32 tile) ----
-    float *A = reinterpret_cast<float *>(sm + I_A);      // [64][AST]
-    float *Inv = reinterpret_cast<float *>(sm + I_INV);  // [64][IST], lower block triangle
+    // A [64][AST] and Inv [64][IST] (lower block triangle): on the fast path A goes over q^ (dead) and Inv over
+    // the [K+; Q+] tile, so that A is written while other warps may still read that tile; the wide-decay path
+    // still reads q^ here and keeps the other order
+    float *A = reinterpret_cast<float *>(sm + (slow ? I_A : I_Q));
+    float *Inv = reinterpret_cast<float *>(sm + (slow ? I_INV : I_A));
     uint8_t *Qks = sm + I_QKS;  // Qk tile staging (read by the copy-out before the next item rewrites it)
     if (ok && !slow) {
         float v[32];
         const int quad = warp & 3, half = (warp >> 2) & 1;  // warps 0-7: lanes 32*quad.., columns 32*half..
-        if (warp < 8) umma::ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * half, v);
-        __syncthreads();  // every warp has read D1 and X1 is no longer read: A may overwrite it
         if (warp < 8) {
+            umma::ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * half, v);
             const int row = 32 * quad + lane;
             if (row < CH) {
 #pragma unroll
@@ -1181,7 +1186,8 @@ __global__ void __launch_bounds__(NTI, 1)
             if (tid < 3 * CC / 8) cw[tid] = wstash[tid];
         }
     }
-    __syncthreads();  // the window stash and this item's metadata are rewritten by the next item
+    // (no barrier: the window stash and this item's metadata are rewritten only after the next item's first
+    // barrier, and thread 0 waits there for the copy-outs that read this item's staging)
     }  // item loop
     if (tid == 0) bulk_wait_all();  // the last item's copy-outs read this CTA's shared memory
     if (!ok && tid == 0) {
