@@ -137,6 +137,42 @@ def test_prefill_matches_oracle_varlen(dk, dv, chunk):
     assert torch.equal(p.pool.conv[keep].view(torch.int16), before_C[keep].view(torch.int16))
 
 
+@pytest.mark.parametrize("dk,dv,chunk,H", [(16, 16, 16, 2), (128, 128, 64, 1)])
+def test_prefill_more_sequences_than_one_table_block(dk, dv, chunk, H):
+    """1500 sequences of 0 to 3 tokens at scattered start positions, a third of them resumed from stored
+    states, checkpoints at every chunk boundary they cross: more sequences than the table kernel's block
+    takes at once, on both paths, against the oracle (outputs, final states, windows, checkpoints)."""
+    kda = _kda()
+    rng = np.random.default_rng(7)
+    N = 1500
+    lens = rng.integers(0, 4, N).tolist()
+    starts = rng.integers(0, 200, N).tolist()
+    src = [N + i if i % 3 == 0 else -1 for i in range(N)]
+    p = Problem(kda, H, dk, dv, lens, starts, src, list(range(N)), chunk, chunk, 2 * N + 64, seed=dk + H)
+    assert len(p.ck) > 0
+    assert p.run() == 0
+    p.check(p.reference())
+
+
+@pytest.mark.parametrize("dk,dv,chunk", [(16, 16, 16), (128, 128, 64)])
+def test_prefill_of_empty_sequences_only(dk, dv, chunk):
+    """A call whose sequences are all empty (no tokens at all): each destination receives its source state and
+    window unchanged (zeros for a fresh one), and no other slot changes."""
+    kda = _kda()
+    src, dst = [3, -1, 5, 1], [2, 4, 6, 7]
+    p = Problem(kda, 2, dk, dv, [0, 0, 0, 0], [0, 9, 64, 100], src, dst, chunk, chunk, 12, seed=dk)
+    before_S, before_C = p.pool.S.clone(), p.pool.conv.clone()
+    assert p.run() == 0
+    for s_, d_ in zip(src, dst):
+        if s_ >= 0:
+            assert torch.equal(p.pool.S[d_], before_S[s_])
+            assert torch.equal(p.pool.conv[d_].view(torch.int16), before_C[s_].view(torch.int16))
+        else:
+            assert not p.pool.S[d_].any() and not p.pool.conv[d_].view(torch.int16).any()
+    keep = [x for x in range(12) if x not in dst]
+    assert torch.equal(p.pool.S[keep], before_S[keep])
+
+
 def test_prefill_no_gate_and_no_checkpoints():
     kda = _kda()
     p = Problem(kda, 2, 128, 128, [100, 37], [0, 64], [-1, 1], [0, 1], 64, 0, 8, seed=5, with_z=False)
