@@ -593,13 +593,13 @@ constexpr uint32_t I_Q = 0, I_K = 32768, I_G = 65536, I_VT = 98304, I_RAW = 1310
 constexpr uint32_t I_X1 = 131072, I_KM = 163840, I_A = 131072, I_T = 163840;
 constexpr uint32_t I_INV = 0;          // Inv fp32 [64][IST] over q^ (free after the Qk copy-out)
 constexpr uint32_t I_MISC = 184320;   // beta, exp(G_mid), decay partial sums, barrier, tmem address, window stash,
-                                      // fp32 q^.k^ per row, G_mid, exp(G_last - G_mid)
+                                      // fp32 q^.k^ per row, G_mid, exp(G_last - G_mid), G row 0
 constexpr uint32_t I_QKS = 192512;    // Qk tf32 staging [64][64]
 constexpr uint32_t I_SMEM = I_QKS + CH * CH * 4 + 1024;  // + alignment slack
 constexpr int RAW_ROWS = CH + kConvW - 1;           // 3 history rows + 64 tokens
 constexpr int AST = 68;                             // row stride of A in smem (padded against bank conflicts)
 constexpr int IST = 68;                             // row stride of Inv in smem (the same padding)
-static_assert(I_A + CH * AST * 4 <= I_T && I_MISC + 7168 <= I_QKS && I_QKS % 1024 == 0, "A, misc, Qk staging");
+static_assert(I_A + CH * AST * 4 <= I_T && I_MISC + 7424 <= I_QKS && I_QKS % 1024 == 0, "A, misc, Qk staging");
 static_assert(I_RAW + RAW_ROWS * 3 * D * 2 <= I_MISC, "raw staging");
 static_assert(I_INV + CH * IST * 4 <= I_K && (IST * 4) % 16 == 0, "Inv staging");
 
@@ -626,6 +626,71 @@ __device__ __forceinline__ float log_sigmoid_fast(float x) {
     return fminf(x, 0.f) - __logf(1.f + __expf(-fabsf(x)));
 }
 
+// Sums of NV values per lane over the 32 lanes of a warp by recursive halving (NV a power of two, 2..32): at each
+// step a lane keeps half of its values, adds the partner's matching half, and passes the other half on.  Lane l
+// returns the total of value l >> (5 - log2 NV); v is overwritten.
+template <int NV>
+__device__ __forceinline__ float warp_reduce_scatter(float *v, int lane) {
+    static_assert(NV >= 2 && NV <= 32 && (NV & (NV - 1)) == 0, "a power of two");
+#pragma unroll
+    for (int n = NV, off = 16; n > 1; n >>= 1, off >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int off = 32 / NV; off > 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off >> 1);
+    return r;
+}
+
+// Packed fp32 pairs (fma / mul / add .f32x2 round each lane as the scalar instruction would).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// two bf16 (low half first) as a packed fp32 pair
+__device__ __forceinline__ uint64_t bf2x2(uint32_t w) { return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
+// x * sigmoid(x) of both lanes with one reciprocal: with y = 1 + exp(-x), 1/y0 = y1 / (y0 y1) and 1/y1 = y0 / (y0 y1).
+// exp(-x) is capped at 2^57 (x below about -39.5, where x sigmoid(x) is below 1e-15 in magnitude) so that the
+// product stays finite.
+__device__ __forceinline__ uint64_t silu2(uint64_t x) {
+    constexpr float kNegLog2e = -1.4426950408889634f;
+    float t0, t1;
+    upk2(mul2(x, pk2(kNegLog2e, kNegLog2e)), t0, t1);
+    float e0, e1;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fminf(t0, 57.f)));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fminf(t1, 57.f)));
+    float y0, y1;
+    upk2(add2(pk2(e0, e1), pk2(1.f, 1.f)), y0, y1);
+    float rp;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rp) : "f"(y0 * y1));
+    return mul2(x, pk2(rp * y1, rp * y0));
+}
+
 __global__ void __launch_bounds__(NTI, 1)
     prefill_intra_tc_kernel(const PrefillArgs a, const Layout2 L, const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -647,7 +712,7 @@ __global__ void __launch_bounds__(NTI, 1)
     uint16_t *astage = reinterpret_cast<uint16_t *>(sm + I_G);  // decay logits bf16 [64][128] (G comes later)
     float *beta = reinterpret_cast<float *>(sm + I_MISC);
     float *eGm = beta + 64;     // exp(G_mid) per channel
-    float *gtot = eGm + D;      // [4][128] partial sums of the cumulative decay
+    float *gtot = eGm + D;      // [128] cumulative decay of tokens 0-31 (the decay sums)
     ItemMeta *meta = reinterpret_cast<ItemMeta *>(sm + I_MISC + 2816);  // [2], by item parity
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + I_MISC + 3072);
     uint64_t *bar_in = bar + 1;
@@ -656,6 +721,7 @@ __global__ void __launch_bounds__(NTI, 1)
     float *qkd = reinterpret_cast<float *>(sm + I_MISC + 5632);      // [64] q^_r . k^_r in fp32
     float *gmid = reinterpret_cast<float *>(sm + I_MISC + 5888);     // [128] G_mid
     float *eglm = reinterpret_cast<float *>(sm + I_MISC + 6400);     // [128] exp(G_last - G_mid)
+    float *g0s = reinterpret_cast<float *>(sm + I_MISC + 6912);      // [128] G row 0
 
     // Item metadata from global memory (one thread; dependent loads).
     // Item metadata: the table kernel's record of the item's chunk (one round of three 16-byte loads).
@@ -704,6 +770,13 @@ __global__ void __launch_bounds__(NTI, 1)
     const int ntok = meta[it & 1].n;
     uint8_t *blk = reinterpret_cast<uint8_t *>(a.ws) + L.off_blk + ((size_t)c * H + h) * WS_BLOCK;
     if (tid == 0) bulk_wait_read_all();  // the item before's -W and U' copy-outs: their staging is rewritten below
+    float4 cw3[3][2];  // conv weights of this thread's three conv units (P1), in flight during the wait below
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const float4 *wp = reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + 2 * ((tid + k * NTI) % (CC / 2))) * kConvW);
+        cw3[k][0] = __ldg(wp);
+        cw3[k][1] = __ldg(wp + 1);
+    }
     ok = !__syncthreads_or(!mbar_wait(bar_in, ph_in));
     if (!ok) break;  // the loads stay in flight: the exit path waits for them once more
     ph_in ^= 1;
@@ -725,40 +798,47 @@ __global__ void __launch_bounds__(NTI, 1)
             __syncthreads();
         }
     }
-    // ---- P1: causal conv + SiLU over (channel, block of 16 rows) units, three per thread: the block's three
-    //      history rows come from the staged raw rows, the window runs in registers along the block ----
-#pragma unroll 1
-    for (int u = tid; u < CC * 4; u += NTI) {
-        const int ch = u % CC, rb = u / CC;
-        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w + ((size_t)h * CC + ch) * kConvW));
-        const uint16_t *rc = raw + (ch >> 7) * RAW_PART + (ch & 127) + 16 * rb * D;  // raw row 16 rb = position -3
-        float h0 = bf2f(rc[0]), h1 = bf2f(rc[D]), h2 = bf2f(rc[2 * D]);
+    // ---- P1: causal conv + SiLU over (channel pair, block of 8 rows) units, three per thread, in packed fp32
+    //      pairs: the block's three history rows come from the staged raw rows, the window runs in registers
+    //      along the block.  A warp's 32 pairs are 64 channels of one of q, k, v. ----
+    static_assert((CC / 2) * (CH / 8) == 3 * NTI && (CC / 2) % 32 == 0, "three conv units per thread");
 #pragma unroll
-        for (int r8 = 0; r8 < 16; r8 += 8) {
-            const int r0 = 16 * rb + r8;
-            float xs8[8], ob[8];
+    for (int k = 0; k < 3; ++k) {
+        const int u = tid + k * NTI, cp = u % (CC / 2), rb = u / (CC / 2);
+        const int part = cp >> 6, cc = 2 * cp - 128 * part, r0 = 8 * rb;
+        const float4 wa = cw3[k][0], wb = cw3[k][1];  // taps of channels cc, cc + 1 (tap 3 on the current row)
+        const uint64_t w0 = pk2(wa.x, wb.x), w1 = pk2(wa.y, wb.y), w2 = pk2(wa.z, wb.z), w3 = pk2(wa.w, wb.w);
+        const uint32_t *rp = reinterpret_cast<const uint32_t *>(raw + part * RAW_PART + r0 * D + cc);  // row r0 = position r0 - 3
+        uint64_t h0 = bf2x2(rp[0]), h1 = bf2x2(rp[D / 2]), h2 = bf2x2(rp[D]);
+        uint64_t ob[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) xs8[k] = bf2f(rc[(r8 + k + 3) * D]);  // all taps before any store
+        for (int kk = 0; kk < 8; ++kk) ob[kk] = bf2x2(rp[(kk + 3) * (D / 2)]);  // all rows before any store
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float x = xs8[k];
-                float out = fmaf(w.w, x, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
-                if (a.silu) out = __fdividef(out, 1.f + __expf(-out));
-                ob[k] = (r0 + k < ntok) ? out : 0.f;
-                h0 = h1;
-                h1 = h2;
-                h2 = x;
-            }
-            if (ch < D) {
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t x = ob[kk];
+            uint64_t out = fma2(w3, x, fma2(w2, h2, fma2(w1, h1, mul2(w0, h0))));
+            ob[kk] = a.silu ? silu2(out) : out;
+            h0 = h1;
+            h1 = h2;
+            h2 = x;
+        }
+        if (r0 + 8 > ntok) {  // the chunk ends inside this block (warp-uniform): rows past it are zero
 #pragma unroll
-                for (int k = 0; k < 8; ++k) qh[(r0 + k) * D + ch] = ob[k];
-            } else if (ch < 2 * D) {
+            for (int kk = 0; kk < 8; ++kk)
+                if (r0 + kk >= ntok) ob[kk] = 0;
+        }
+        if (part < 2) {
+            float *dstp = (part == 0 ? qh : kh) + r0 * D + cc;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) kh[(r0 + k) * D + ch - D] = ob[k];
-            } else {
-                umma::st_tf32x4(Vt, D, ch - 2 * D, r0, ob[0], ob[1], ob[2], ob[3]);
-                umma::st_tf32x4(Vt, D, ch - 2 * D, r0 + 4, ob[4], ob[5], ob[6], ob[7]);
-            }
+            for (int kk = 0; kk < 8; ++kk) *reinterpret_cast<uint64_t *>(dstp + kk * D) = ob[kk];
+        } else {
+            float lo[8], hi[8];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) upk2(ob[kk], lo[kk], hi[kk]);
+            umma::st_tf32x4(Vt, D, cc, r0, lo[0], lo[1], lo[2], lo[3]);
+            umma::st_tf32x4(Vt, D, cc, r0 + 4, lo[4], lo[5], lo[6], lo[7]);
+            umma::st_tf32x4(Vt, D, cc + 1, r0, hi[0], hi[1], hi[2], hi[3]);
+            umma::st_tf32x4(Vt, D, cc + 1, r0 + 4, hi[4], hi[5], hi[6], hi[7]);
         }
     }
     __syncthreads();
@@ -767,57 +847,34 @@ __global__ void __launch_bounds__(NTI, 1)
         const int r3 = tid / (CC / 8), rem = tid - r3 * (CC / 8), part = rem >> 4, unit = rem & 15;
         wstash[tid] = reinterpret_cast<const uint4 *>(raw + part * RAW_PART + (ntok + r3) * D)[unit];
     }
-    {   // L2 norms: rows warp, warp + 16, warp + 32, warp + 48, their reductions interleaved; the values stay
-        // in registers between the sums and the scaling
-        float sq[4], sk[4], vq[4][D / 32], vk[4][D / 32];
+    {   // L2 norms of q and k rows 4 warp .. 4 warp + 3 (lane: channels 4 lane .. 4 lane + 3 of each), and q^.k^
+        const int rw = 4 * warp;
+        float4 vq[4], vk[4];
+        float ss[8];
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const int r = warp + 16 * k4;
-            float aq = 0.f, ak = 0.f;
-#pragma unroll
-            for (int i = 0; i < D / 32; ++i) {
-                const float xq = qh[r * D + lane + 32 * i], xk = kh[r * D + lane + 32 * i];
-                vq[k4][i] = xq;
-                vk[k4][i] = xk;
-                aq = fmaf(xq, xq, aq);
-                ak = fmaf(xk, xk, ak);
-            }
-            sq[k4] = aq;
-            sk[k4] = ak;
+        for (int j = 0; j < 4; ++j) {
+            vq[j] = *reinterpret_cast<const float4 *>(qh + (rw + j) * D + 4 * lane);
+            vk[j] = *reinterpret_cast<const float4 *>(kh + (rw + j) * D + 4 * lane);
+            ss[2 * j] = fmaf(vq[j].w, vq[j].w, fmaf(vq[j].z, vq[j].z, fmaf(vq[j].y, vq[j].y, vq[j].x * vq[j].x)));
+            ss[2 * j + 1] = fmaf(vk[j].w, vk[j].w, fmaf(vk[j].z, vk[j].z, fmaf(vk[j].y, vk[j].y, vk[j].x * vk[j].x)));
         }
+        const float rs = rsqrtf(warp_reduce_scatter<8>(ss, lane) + a.l2_eps);  // lane l: row l / 8, k if l % 8 >= 4
+        float dq[4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                sq[k4] += __shfl_xor_sync(0xffffffffu, sq[k4], o);
-                sk[k4] += __shfl_xor_sync(0xffffffffu, sk[k4], o);
+        for (int j = 0; j < 4; ++j) {
+            const float rq = __shfl_sync(0xffffffffu, rs, 8 * j), rk = __shfl_sync(0xffffffffu, rs, 8 * j + 4);
+            vq[j].x *= rq; vq[j].y *= rq; vq[j].z *= rq; vq[j].w *= rq;
+            vk[j].x *= rk; vk[j].y *= rk; vk[j].z *= rk; vk[j].w *= rk;
+            dq[j] = fmaf(vq[j].w, vk[j].w, fmaf(vq[j].z, vk[j].z, fmaf(vq[j].y, vk[j].y, vq[j].x * vk[j].x)));
+            if (rw + j < ntok) {
+                *reinterpret_cast<float4 *>(qh + (rw + j) * D + 4 * lane) = vq[j];
+                *reinterpret_cast<float4 *>(kh + (rw + j) * D + 4 * lane) = vk[j];
             }
-        float dqk[4];  // q^_r . k^_r of the stored (normalised, fp32) vectors; rows past the chunk's end are 0
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const int r = warp + 16 * k4;
-            const float rq = rsqrtf(sq[k4] + a.l2_eps), rk = rsqrtf(sk[k4] + a.l2_eps);
-            float dd = 0.f;
-#pragma unroll
-            for (int i = 0; i < D / 32; ++i) {
-                const float qn = vq[k4][i] * rq, kn = vk[k4][i] * rk;
-                dd = fmaf(qn, kn, dd);
-                if (r < ntok) {
-                    qh[r * D + lane + 32 * i] = qn;
-                    kh[r * D + lane + 32 * i] = kn;
-                }
-            }
-            dqk[k4] = dd;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) dqk[k4] += __shfl_xor_sync(0xffffffffu, dqk[k4], o);
-        if (lane == 0) {
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) qkd[warp + 16 * k4] = warp + 16 * k4 < ntok ? dqk[k4] : 0.f;
-        }
+        const float dqk = warp_reduce_scatter<4>(dq, lane);  // lane l: row l / 8
+        if ((lane & 7) == 0) qkd[rw + (lane >> 3)] = rw + (lane >> 3) < ntok ? dqk : 0.f;
     }
+    bool wide = false;
     {   // cumulative log decay along the chunk from the staged logits: 4 threads per channel, 16 tokens each,
         // in registers; G overwrites the staging only after every logit has been read
         const int ch = tid & 127, qd = tid >> 7;
@@ -830,26 +887,27 @@ __global__ void __launch_bounds__(NTI, 1)
             g16[u] = acc;
         }
         gtot[qd * D + ch] = acc;
+        if (qd == 0) g0s[ch] = g16[0];
         __syncthreads();
         float off = 0.f;
         for (int q2 = 0; q2 < qd; ++q2) off += gtot[q2 * D + ch];
 #pragma unroll
         for (int u = 0; u < 16; ++u) G[(16 * qd + u) * D + ch] = qd > 0 ? g16[u] + off : g16[u];
-    }
-    __syncthreads();
-
-    // ---- P2: [K+;Q+] and K- with a mid-chunk reference; Q+ tile to the workspace ----
-    constexpr int MID = CH / 2;
-    bool wide = false;
-    if (tid < D) {
-        const float g0 = G[tid], gm = G[MID * D + tid], gl = G[(CH - 1) * D + tid];
-        wide = (g0 - gm > kMidRange) || (gm - gl > kMidRange);
-        eGm[tid] = expf(gm);
-        gmid[tid] = gm;
-        eglm[tid] = expf(gl - gm);
-        reinterpret_cast<float *>(blk + WS_GL)[tid] = expf(gl);
+        static_assert(CH / 2 == 32, "G_mid is the first row of the third quarter");
+        if (qd == 2) {
+            // the mid-chunk reference G_mid = G row 32 and G_last = G row 63 of this channel, each summed exactly
+            // as its row of G is above, and whether the chunk's decay range is too wide for one reference
+            const float gm = g16[0] + off, gl = gtot[3 * D + ch] + (off + gtot[2 * D + ch]);
+            wide = (g0s[ch] - gm > kMidRange) || (gm - gl > kMidRange);
+            eGm[ch] = expf(gm);
+            gmid[ch] = gm;
+            eglm[ch] = expf(gl - gm);
+            reinterpret_cast<float *>(blk + WS_GL)[ch] = expf(gl);
+        }
     }
     const bool slow = __syncthreads_or(wide) != 0;
+
+    // ---- P2: [K+;Q+] and K- with a mid-chunk reference; Q+ tile to the workspace ----
     uint8_t *X1 = sm + I_X1;  // [K+; Q+] tf32 [128 rows][64 channels] of one channel half
     uint8_t *Km = sm + I_KM;  // K- tf32 [64 rows][64 channels] of one channel half
     {   // The [A; Qk] MMA takes tf32 operands and runs in two channel halves whose tiles take the space of one
@@ -861,7 +919,7 @@ __global__ void __launch_bounds__(NTI, 1)
         float xk[4][2], xq[4][2], xm[4][2];  // K+, Q+ (mid reference), K- of the thread's rows and channels
         auto form = [&](int hh) {  // ... of channel half hh; Q+ (chunk start) of that half to the workspace
             const int ic = 64 * hh + c2;
-            const float2 m2 = *reinterpret_cast<const float2 *>(gmid + ic);  // (row MID of G is overwritten below)
+            const float2 m2 = *reinterpret_cast<const float2 *>(gmid + ic);  // (row 32 of G is overwritten below)
             const float2 e2 = *reinterpret_cast<const float2 *>(eGm + ic);
             const float gmv[2] = {m2.x, m2.y}, egv[2] = {e2.x, e2.y};
 #pragma unroll

@@ -48,9 +48,11 @@ __device__ __forceinline__ void st_tf32x4(uint8_t *tile, int R, int r, int k0, f
                                                                               to_tf32(x3));
 }
 
+// two floats rounded to bf16 (nearest even) in one conversion, lo in the low half
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 __device__ __forceinline__ void st_bf16x8(uint8_t *tile, int R, int r, int k0, const float *x) {
