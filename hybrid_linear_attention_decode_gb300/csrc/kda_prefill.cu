@@ -672,18 +672,21 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 // two bf16 (low half first) as a packed fp32 pair
 __device__ __forceinline__ uint64_t bf2x2(uint32_t w) { return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
 // x * sigmoid(x) of both lanes with one reciprocal: with y = 1 + exp(-x), 1/y0 = y1 / (y0 y1) and 1/y1 = y0 / (y0 y1).
 // exp(-x) is capped at 2^57 (x below about -39.5, where x sigmoid(x) is below 1e-15 in magnitude) so that the
 // product stays finite.
 __device__ __forceinline__ uint64_t silu2(uint64_t x) {
-    constexpr float kNegLog2e = -1.4426950408889634f;
     float t0, t1;
-    upk2(mul2(x, pk2(kNegLog2e, kNegLog2e)), t0, t1);
-    float e0, e1;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fminf(t0, 57.f)));
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fminf(t1, 57.f)));
+    upk2(mul2(x, pk2(-kLog2e, -kLog2e)), t0, t1);
+    const float e0 = ex2_approx(fminf(t0, 57.f)), e1 = ex2_approx(fminf(t1, 57.f));
     float y0, y1;
     upk2(add2(pk2(e0, e1), pk2(1.f, 1.f)), y0, y1);
     float rp;
@@ -918,39 +921,42 @@ __global__ void __launch_bounds__(NTI, 1)
         const int c2 = 2 * lane;
         float xk[4][2], xq[4][2], xm[4][2];  // K+, Q+ (mid reference), K- of the thread's rows and channels
         auto form = [&](int hh) {  // ... of channel half hh; Q+ (chunk start) of that half to the workspace
+            // (packed pairs of the thread's two channels: exp(G - G_mid) and exp(G_mid - G) share one argument)
             const int ic = 64 * hh + c2;
             const float2 m2 = *reinterpret_cast<const float2 *>(gmid + ic);  // (row 32 of G is overwritten below)
             const float2 e2 = *reinterpret_cast<const float2 *>(eGm + ic);
-            const float gmv[2] = {m2.x, m2.y}, egv[2] = {e2.x, e2.y};
+            const uint64_t ngm2 = pk2(-m2.x, -m2.y), eg2 = pk2(e2.x, e2.y);
+            const uint64_t l2e2 = pk2(kLog2e, kLog2e), sc2 = pk2(a.scale, a.scale);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int r = warp + 16 * j;
-                const float2 g2 = *reinterpret_cast<const float2 *>(G + r * D + ic);
-                const float2 k2 = *reinterpret_cast<const float2 *>(kh + r * D + ic);
-                const float2 q2 = *reinterpret_cast<const float2 *>(qh + r * D + ic);
-                const float gv[2] = {g2.x, g2.y}, kv[2] = {k2.x, k2.y}, qv[2] = {q2.x, q2.y};
-                float xp[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const float g = gv[u], k_ = kv[u], q_ = qv[u];
-                    float eq;
-                    if (!slow) {
-                        const float ep = __expf(g - gmv[u]);
-                        xk[j][u] = k_ * ep;
-                        xq[j][u] = q_ * ep;
-                        xm[j][u] = k_ * __expf(gmv[u] - g);
-                        eq = ep * egv[u];
-                    } else {
-                        xk[j][u] = xq[j][u] = xm[j][u] = 0.f;
-                        eq = __expf(g);
-                    }
-                    xp[u] = a.scale * q_ * eq;
+                const uint64_t g2 = *reinterpret_cast<const uint64_t *>(G + r * D + ic);
+                const uint64_t k2 = *reinterpret_cast<const uint64_t *>(kh + r * D + ic);
+                const uint64_t q2 = *reinterpret_cast<const uint64_t *>(qh + r * D + ic);
+                uint64_t xk2 = 0, xq2 = 0, xm2 = 0, eq2;
+                if (!slow) {
+                    float t0, t1;
+                    upk2(mul2(add2(g2, ngm2), l2e2), t0, t1);  // (G - G_mid) log2(e)
+                    const uint64_t ep2 = pk2(ex2_approx(t0), ex2_approx(t1));
+                    const uint64_t em2 = pk2(ex2_approx(-t0), ex2_approx(-t1));
+                    xk2 = mul2(k2, ep2);
+                    xq2 = mul2(q2, ep2);
+                    xm2 = mul2(k2, em2);
+                    eq2 = mul2(ep2, eg2);
+                } else {
+                    float g0, g1;
+                    upk2(g2, g0, g1);
+                    eq2 = pk2(__expf(g0), __expf(g1));
                 }
-                *reinterpret_cast<uint32_t *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, ic)) =
-                    umma::pack_bf16(xp[0], xp[1]);
+                float xp0, xp1;
+                upk2(mul2(mul2(sc2, q2), eq2), xp0, xp1);
+                *reinterpret_cast<uint32_t *>(blk + WS_QP + umma::sw128_offset<2>(CH, r, ic)) = umma::pack_bf16(xp0, xp1);
+                upk2(xk2, xk[j][0], xk[j][1]);
+                upk2(xq2, xq[j][0], xq[j][1]);
+                upk2(xm2, xm[j][0], xm[j][1]);
                 if (!slow) {  // fp32 K+ and K- for P5, over the k^ and G they were formed from
-                    *reinterpret_cast<float2 *>(kh + r * D + ic) = make_float2(xk[j][0], xk[j][1]);
-                    *reinterpret_cast<float2 *>(G + r * D + ic) = make_float2(xm[j][0], xm[j][1]);
+                    *reinterpret_cast<uint64_t *>(kh + r * D + ic) = xk2;
+                    *reinterpret_cast<uint64_t *>(G + r * D + ic) = xm2;
                 }
             }
         };
@@ -1268,11 +1274,12 @@ constexpr uint32_t S_UT32 = 148480;   // U^T tf32 tile [128 j][64 r]: A operand 
 constexpr uint32_t S_OST = 181248;    // O staging fp32 [64 r][OST] of the output warps (row stride 132: conflict-free)
 constexpr int OST = 132;
 constexpr uint32_t S_NW = 215040;     // RMSNorm weight [128]
-constexpr uint32_t S_GLN = 215552;    // exp(G_last) of the next chunk [128]
-constexpr uint32_t S_MISC = 216064;   // barriers, tensor-memory address
+constexpr uint32_t S_GLN = 215552;    // exp(G_last) of chunk c [2][128], by chunk parity
+constexpr uint32_t S_MISC = 216576;   // barriers, tensor-memory address
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
 static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0, "state smem layout");
 static_assert(S_UT32 + D * CH * 4 <= S_OST && S_OST + CH * OST * 4 <= S_NW, "state smem layout");
+static_assert(S_NW + D * 4 <= S_GLN && S_GLN + 2 * D * 4 <= S_MISC, "state smem layout");
 constexpr int NCW = 8;                // chain warps: two per tensor-memory lane quadrant
 constexpr int NOW = 8;                // output warps: two per lane quadrant
 constexpr int NTS = 32 * (NCW + NOW);
@@ -1451,6 +1458,40 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         int ck_pre = (want_ck && next_b <= send) ? cks[jck] : -1;
         ChunkEnt e_nx = !empty ? ent[cb] : ChunkEnt{};
         int64_t p_nx = pb;
+        int ck_prev = -1;  // checkpoint slot of the chunk before's end
+        // The state pass of a chunk (key channels i0 .. i0 + 63 of S^T, in tensor memory) after its bf16 tile:
+        // the checkpoint, then S^T diag(exp(G_last of the next chunk)) back to tensor memory when a chunk follows
+        // in this launch (gl: its exp(G_last)), else the state to the destination slot or to the carry.
+        auto s_rest = [&](int ckp, const float *gl) {
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+                const int ig = i0 + 32 * g;
+                uint32_t r[32];
+                umma::ld32_issue(tmem + lane_off + T_S + ig, r);
+                umma::wait_ld(r);
+                float v[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
+                if (ckp >= 0) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        store_state(a.S, a.state_bf16, (((size_t)ckp * H + h) * D + ig + t) * D + j, v[t]);
+                }
+                if (gl) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) v[t] *= gl[ig + t];
+                    umma::st32_issue(tmem + lane_off + T_S + ig, v);
+                } else if (last) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + ig + t) * D + j, v[t]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) carry[(size_t)(ig + t) * D + j] = v[t];
+                }
+            }
+            umma::wait_st();
+        };
         for (int32_t c = cb; c < ce; ++c) {
             const ChunkEnt e = e_nx;
             const int ob = (c - cb) & 1;                        // O^T buffer of this chunk
@@ -1492,6 +1533,9 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 }
             }
             ph_w ^= 1;
+            // the rest of the state pass of the chunk before, while the MMAs above run: its checkpoint, and
+            // S^T diag(exp(G_last of this chunk)) back to tensor memory for this chunk's S^T MMA
+            if (c > cb) s_rest(ck_prev, gln + (c & 1) * D);
             // each thread waits for U^T itself; a timed-out wait is voted on at the barrier after the U tiles
             ok = mbar_wait(bar_mma, ph_m);
             ph_m ^= 1;
@@ -1520,7 +1564,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 for (int t = 0; t < 32; t += 4)
                     umma::st_tf32x4(Ut32, D, j, r0 + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
             }
-            if (tid < D) gln[tid] = gnext;
+            if (tid < D) gln[((c + 1) & 1) * D + tid] = gnext;
             fence_proxy_async_smem();
             umma::fence_before();
             ok = !state_sync_or(!(ok && t0ok));
@@ -1557,39 +1601,21 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             ph_m ^= 1;
             umma::fence_after();
             if (tid == 0 && ok && has_next) issue_qp(c + 1);  // every MMA before the S^T commit is done: Q+ is free
-            // ---- S pass (this thread: key channels i0 .. i0 + 63, in two groups of 32): bf16 tile of the new
-            //      state, checkpoint, then decay by the next chunk (or the final store) ----
-            if (ok) {
-                auto s_part = [&](int ig) {
+            // ---- S pass, the part the next chunk's first MMAs wait for (this thread: key channels i0 .. i0 + 63):
+            //      the bf16 operand tile of the new state.  The rest (checkpoint, decay, final store) follows the
+            //      barrier below, or the next chunk's MMA issue. ----
+            if (ok && has_next) {
+#pragma unroll 1
+                for (int g = 0; g < 2; ++g) {
                     uint32_t r[32];
-                    umma::ld32_issue(tmem + lane_off + T_S + ig, r);
+                    umma::ld32_issue(tmem + lane_off + T_S + i0 + 32 * g, r);
                     umma::wait_ld(r);
                     float v[32];
 #pragma unroll
                     for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
-                    if (ck >= 0) {
 #pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            store_state(a.S, a.state_bf16, (((size_t)ck * H + h) * D + ig + t) * D + j, v[t]);
-                    }
-                    if (has_next) {
-#pragma unroll
-                        for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, ig + t, v + t);
-#pragma unroll
-                        for (int t = 0; t < 32; ++t) v[t] *= gln[ig + t];
-                        umma::st32_issue(tmem + lane_off + T_S + ig, v);
-                    } else if (last) {
-#pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            store_state(a.S, a.state_bf16, (((size_t)dst * H + h) * D + ig + t) * D + j, v[t]);
-                    } else {
-#pragma unroll
-                        for (int t = 0; t < 32; ++t) carry[(size_t)(ig + t) * D + j] = v[t];
-                    }
-                };
-                s_part(i0);
-                s_part(i0 + 32);
-                umma::wait_st();
+                    for (int t = 0; t < 32; t += 8) umma::st_bf16x8(Sst, D, j, i0 + 32 * g + t, v + t);
+                }
             }
             // Qk and Ktil^T of the next chunk, once the O^T MMAs that read Qk are done (thread 0; the S^T MMAs
             // that read Ktil^T are)
@@ -1607,7 +1633,9 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             ok = !state_sync_or(!(ok && t0ok));
             umma::fence_after();
             if (!ok) break;
+            ck_prev = ck;
         }
+        if (ok && ce > cb) s_rest(ck_prev, nullptr);  // the last chunk's checkpoint and the final (or carried) state
         if (!ok && tid == 0) {
             set_status(a.status, KDA_DEV_TIMEOUT);
             // copies still in flight into this CTA's shared memory land before it exits (short bounded waits;
