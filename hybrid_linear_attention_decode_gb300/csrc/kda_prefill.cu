@@ -1335,13 +1335,14 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     float *Ost = reinterpret_cast<float *>(sm + S_OST);
     float *nw = reinterpret_cast<float *>(sm + S_NW);
     float *gln = reinterpret_cast<float *>(sm + S_GLN);
-    uint64_t *bar_w = reinterpret_cast<uint64_t *>(sm + S_MISC);  // -W and Q+ of a chunk
+    uint64_t *bar_w = reinterpret_cast<uint64_t *>(sm + S_MISC);  // -W of a chunk
     uint64_t *bar_u = bar_w + 1;                                    // U'
     uint64_t *bar_b = bar_w + 2;                                    // Qk and Ktil^T (+ exp(G_last))
     uint64_t *bar_mma = bar_w + 3;                                  // the U^T and the S^T MMAs
     uint64_t *bar_o = bar_w + 4;      // [2] the O^T MMAs of a chunk into buffer b
     uint64_t *bar_ofree = bar_w + 6;  // [2] buffer b read by the output warps (one arrival per output warp)
-    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 64);
+    uint64_t *bar_q = bar_w + 8;      // Q+ of a chunk
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 128);
     const int64_t start = a.start_pos[n];
     const int32_t c0 = wsp<int32_t>(a, L.off_seqc)[n], c1 = wsp<int32_t>(a, L.off_seqc)[n + 1];
     // this launch's chunks of the sequence: [cb, ce) = [c0, c1) within [seg_lo, seg_hi).  The state enters
@@ -1357,13 +1358,17 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     const int64_t *pos = wsp<int64_t>(a, L.off_pos);
     const uint8_t *blk0 = reinterpret_cast<const uint8_t *>(a.ws) + L.off_blk;
     auto blk_of = [&](int32_t c) { return blk0 + ((size_t)c * H + h) * WS_BLOCK; };
-    // -W and Q+ complete one phase of bar_w together: -W is copied as soon as the U^T MMAs are done with
-    // it, Q+ once every MMA of the chunk before the S^T commit is (the O^T MMAs that read it precede it)
+    // -W is copied as soon as the U^T MMAs are done with it, Q+ once every MMA of the chunk before the S^T
+    // commit is (the O^T MMAs that read it precede it); each has its own barrier, so that the U^T MMAs of a
+    // chunk need not wait for Q+
     auto issue_w = [&](int32_t c) {
-        mbar_arrive_expect_tx(bar_w, 2 * CH * D * 2);
+        mbar_arrive_expect_tx(bar_w, CH * D * 2);
         bulk_g2s(ops + WS_W, blk_of(c) + WS_W, CH * D * 2, bar_w);
     };
-    auto issue_qp = [&](int32_t c) { bulk_g2s(ops + WS_QP, blk_of(c) + WS_QP, CH * D * 2, bar_w); };
+    auto issue_qp = [&](int32_t c) {
+        mbar_arrive_expect_tx(bar_q, CH * D * 2);
+        bulk_g2s(ops + WS_QP, blk_of(c) + WS_QP, CH * D * 2, bar_q);
+    };
     auto issue_u = [&](int32_t c) {
         mbar_arrive_expect_tx(bar_u, CH * D * 4);
         bulk_g2s(ops + WS_UP, blk_of(c) + WS_UP, CH * D * 4, bar_u);
@@ -1376,12 +1381,13 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
 
     // thread 0's record of the copies it issued and has not yet seen complete, with the parity of the phase
     // that completes each (read only on the exit after a timed-out wait)
-    bool out_w = false, out_u = false, out_b = false;
-    uint32_t par_w = 0, par_u = 0, par_b = 0;
+    bool out_w = false, out_u = false, out_b = false, out_q = false;
+    uint32_t par_w = 0, par_u = 0, par_b = 0, par_q = 0;
     if (warp == 0) umma::alloc(tmem_s, T_COLS);
     for (int jj = tid; jj < D; jj += NTS) nw[jj] = __ldg(a.norm_w + jj);
     if (tid == 0) {
         for (int b = 0; b < 4; ++b) mbar_init(bar_w + b, 1);
+        mbar_init(bar_q, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_o + b, 1);
             mbar_init(bar_ofree + b, NOW);
@@ -1392,7 +1398,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             issue_qp(cb);
             issue_u(cb);
             issue_b(cb);
-            out_w = out_u = out_b = true;
+            out_w = out_u = out_b = out_q = true;
         }
     }
     umma::fence_before();
@@ -1444,7 +1450,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         umma::fence_before();
         state_sync();
         umma::fence_after();
-        uint32_t ph_w = 0, ph_u = 0, ph_b = 0, ph_m = 0;
+        uint32_t ph_w = 0, ph_u = 0, ph_b = 0, ph_m = 0, ph_q = 0;
         bool ok = true, t0ok = true;  // t0ok: thread 0's waits on the output warps' buffer releases
         // checkpoint boundaries: a running next boundary, its slot fetched one boundary ahead (no division in
         // the loop); chunk entries are fetched one chunk ahead
@@ -1479,7 +1485,13 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 }
                 if (gl) {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] *= gl[ig + t];
+                    for (int t = 0; t < 32; t += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(gl + ig + t);
+                        v[t] *= g4.x;
+                        v[t + 1] *= g4.y;
+                        v[t + 2] *= g4.z;
+                        v[t + 3] *= g4.w;
+                    }
                     umma::st32_issue(tmem + lane_off + T_S + ig, v);
                 } else if (last) {
 #pragma unroll
@@ -1511,18 +1523,30 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             }
             const float gnext = (tid < D && has_next) ? __ldg(reinterpret_cast<const float *>(blk_of(c + 1) + WS_GL) + tid)
                                                       : 1.f;
-            // ---- U^T = S^T (-W)^T; then, once the output warps have read this O^T buffer (two chunks ago),
-            //      O^T = S^T Q+^T.  If -W / Q+ never arrive, nothing is committed and every thread's bounded wait
+            // ---- U^T = S^T (-W)^T.  If -W never arrives, nothing is committed and every thread's bounded wait
             //      on bar_mma gives up ----
+            const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
+            const uint64_t dS = umma::sdesc_k(Sst, D, 0);
+            bool issued = false;
             if (tid == 0 && mbar_wait(bar_w, ph_w)) {
                 out_w = false;
-                const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
-                const uint64_t dS = umma::sdesc_k(Sst, D, 0), dW = umma::sdesc_k(ops + WS_W, CH, 0);
+                const uint64_t dW = umma::sdesc_k(ops + WS_W, CH, 0);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     umma::mma_bf16(tmem + T_U, umma::sdesc_at(dS, D, ks), umma::sdesc_at(dW, CH, ks), idp, ks > 0);
-                umma::commit(bar_mma);  // U^T is read back first; the O^T MMAs complete meanwhile
-                if (c - cb >= 2 && !mbar_wait(bar_ofree + ob, opar ^ 1u)) t0ok = false;
+                umma::commit(bar_mma);
+                issued = true;
+            }
+            ph_w ^= 1;
+            // the rest of the state pass of the chunk before, while the MMAs above run: its checkpoint, and
+            // S^T diag(exp(G_last of this chunk)) back to tensor memory for this chunk's S^T MMA
+            if (c > cb) s_rest(ck_prev, gln + (c & 1) * D);
+            // ---- once Q+ is in and the output warps have read this O^T buffer (two chunks ago):
+            //      O^T = S^T Q+^T (the S^T commit below covers it) ----
+            if (tid == 0 && issued) {
+                const bool okq = mbar_wait(bar_q, ph_q);
+                if (okq) out_q = false;
+                if (!okq || (c - cb >= 2 && !mbar_wait(bar_ofree + ob, opar ^ 1u))) t0ok = false;
                 umma::fence_after();
                 if (t0ok) {
                     const uint32_t tob = tmem + T_O + 64u * (uint32_t)ob;
@@ -1532,10 +1556,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                         umma::mma_bf16(tob, umma::sdesc_at(dS, D, ks), umma::sdesc_at(dQ, CH, ks), idp, ks > 0);
                 }
             }
-            ph_w ^= 1;
-            // the rest of the state pass of the chunk before, while the MMAs above run: its checkpoint, and
-            // S^T diag(exp(G_last of this chunk)) back to tensor memory for this chunk's S^T MMA
-            if (c > cb) s_rest(ck_prev, gln + (c & 1) * D);
+            ph_q ^= 1;
             // each thread waits for U^T itself; a timed-out wait is voted on at the barrier after the U tiles
             ok = mbar_wait(bar_mma, ph_m);
             ph_m ^= 1;
@@ -1565,6 +1586,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                     umma::st_tf32x4(Ut32, D, j, r0 + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
             }
             if (tid < D) gln[((c + 1) & 1) * D + tid] = gnext;
+
             fence_proxy_async_smem();
             umma::fence_before();
             ok = !state_sync_or(!(ok && t0ok));
@@ -1600,7 +1622,12 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_m));
             ph_m ^= 1;
             umma::fence_after();
-            if (tid == 0 && ok && has_next) issue_qp(c + 1);  // every MMA before the S^T commit is done: Q+ is free
+            if (tid == 0 && ok && has_next) {  // every MMA before the S^T commit is done: Q+ is free
+                issue_qp(c + 1);
+                out_q = true;
+                par_q = ph_q;
+            }
+
             // ---- S pass, the part the next chunk's first MMAs wait for (this thread: key channels i0 .. i0 + 63):
             //      the bf16 operand tile of the new state.  The rest (checkpoint, decay, final store) follows the
             //      barrier below, or the next chunk's MMA issue. ----
@@ -1638,10 +1665,10 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         if (ok && ce > cb) s_rest(ck_prev, nullptr);  // the last chunk's checkpoint and the final (or carried) state
         if (!ok && tid == 0) {
             set_status(a.status, KDA_DEV_TIMEOUT);
-            // copies still in flight into this CTA's shared memory land before it exits (short bounded waits;
-            // the -W / Q+ phase never completes if Q+ was not issued, and that wait just runs out)
+            // copies still in flight into this CTA's shared memory land before it exits (short bounded waits)
             constexpr uint64_t kDrainNs = 10000000ull;
             if (out_w) mbar_wait(bar_w, par_w, kDrainNs);
+            if (out_q) mbar_wait(bar_q, par_q, kDrainNs);
             if (out_u) mbar_wait(bar_u, par_u, kDrainNs);
             if (out_b) mbar_wait(bar_b, par_b, kDrainNs);
         }
