@@ -1271,14 +1271,16 @@ namespace tc {
 constexpr uint32_t S_ST = 0;          // S^T bf16 tile [128 j][128 i]: A operand of U^T = S^T (-W)^T, O^T = S^T Q+^T
 constexpr uint32_t S_OPS = 32768;     // one chunk's workspace block (Qk, -W, Q+, Ktil^T, gl, U'), WS_BLOCK bytes
 constexpr uint32_t S_UT32 = 148480;   // U^T tf32 tile [128 j][64 r]: A operand of S^T += U^T Ktil, O^T += U^T Qk^T
-constexpr uint32_t S_OST = 181248;    // O staging fp32 [64 r][OST] of the output warps (row stride 132: conflict-free)
-constexpr int OST = 132;
+constexpr uint32_t S_OST = 181248;    // O staging fp32 [32 r][OST] of the output warps, half a chunk at a time
+constexpr int OST = 132;              // (row stride 132: conflict-free)
+constexpr uint32_t S_QP2 = 198656;    // the second Q+ buffer (the first is in the chunk block): bf16 [64 r][128 i]
 constexpr uint32_t S_NW = 215040;     // RMSNorm weight [128]
 constexpr uint32_t S_GLN = 215552;    // exp(G_last) of chunk c [2][128], by chunk parity
 constexpr uint32_t S_MISC = 216576;   // barriers, tensor-memory address
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
 static_assert(S_OPS + WS_BLOCK <= S_UT32 && S_UT32 % 1024 == 0, "state smem layout");
-static_assert(S_UT32 + D * CH * 4 <= S_OST && S_OST + CH * OST * 4 <= S_NW, "state smem layout");
+static_assert(S_UT32 + D * CH * 4 <= S_OST && S_OST + 32 * OST * 4 <= S_QP2, "state smem layout");
+static_assert(S_QP2 % 1024 == 0 && S_QP2 + CH * D * 2 <= S_NW, "state smem layout");
 static_assert(S_NW + D * 4 <= S_GLN && S_GLN + 2 * D * 4 <= S_MISC, "state smem layout");
 constexpr int NCW = 8;                // chain warps: two per tensor-memory lane quadrant
 constexpr int NOW = 8;                // output warps: two per lane quadrant
@@ -1341,8 +1343,9 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     uint64_t *bar_mma = bar_w + 3;                                  // the U^T and the S^T MMAs
     uint64_t *bar_o = bar_w + 4;      // [2] the O^T MMAs of a chunk into buffer b
     uint64_t *bar_ofree = bar_w + 6;  // [2] buffer b read by the output warps (one arrival per output warp)
-    uint64_t *bar_q = bar_w + 8;      // Q+ of a chunk
+    uint64_t *bar_q = bar_w + 8;      // [2] Q+ of a chunk in buffer b (chunk c of this launch: b = (c - cb) & 1)
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(sm + S_MISC + 128);
+    auto qpbuf = [&](int b) { return b ? sm + S_QP2 : ops + WS_QP; };
     const int64_t start = a.start_pos[n];
     const int32_t c0 = wsp<int32_t>(a, L.off_seqc)[n], c1 = wsp<int32_t>(a, L.off_seqc)[n + 1];
     // this launch's chunks of the sequence: [cb, ce) = [c0, c1) within [seg_lo, seg_hi).  The state enters
@@ -1358,16 +1361,17 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
     const int64_t *pos = wsp<int64_t>(a, L.off_pos);
     const uint8_t *blk0 = reinterpret_cast<const uint8_t *>(a.ws) + L.off_blk;
     auto blk_of = [&](int32_t c) { return blk0 + ((size_t)c * H + h) * WS_BLOCK; };
-    // -W is copied as soon as the U^T MMAs are done with it, Q+ once every MMA of the chunk before the S^T
-    // commit is (the O^T MMAs that read it precede it); each has its own barrier, so that the U^T MMAs of a
-    // chunk need not wait for Q+
+    // -W is copied as soon as the U^T MMAs are done with it.  Q+ has two buffers, so that the Q+ of chunk
+    // c + 2 is copied once the S^T commit of chunk c (which covers the O^T MMAs that read its buffer) is seen:
+    // it is in place when its chunk starts
     auto issue_w = [&](int32_t c) {
         mbar_arrive_expect_tx(bar_w, CH * D * 2);
         bulk_g2s(ops + WS_W, blk_of(c) + WS_W, CH * D * 2, bar_w);
     };
     auto issue_qp = [&](int32_t c) {
-        mbar_arrive_expect_tx(bar_q, CH * D * 2);
-        bulk_g2s(ops + WS_QP, blk_of(c) + WS_QP, CH * D * 2, bar_q);
+        const int b = (c - cb) & 1;
+        mbar_arrive_expect_tx(bar_q + b, CH * D * 2);
+        bulk_g2s(qpbuf(b), blk_of(c) + WS_QP, CH * D * 2, bar_q + b);
     };
     auto issue_u = [&](int32_t c) {
         mbar_arrive_expect_tx(bar_u, CH * D * 4);
@@ -1381,13 +1385,15 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
 
     // thread 0's record of the copies it issued and has not yet seen complete, with the parity of the phase
     // that completes each (read only on the exit after a timed-out wait)
-    bool out_w = false, out_u = false, out_b = false, out_q = false;
-    uint32_t par_w = 0, par_u = 0, par_b = 0, par_q = 0;
+    bool out_w = false, out_u = false, out_b = false;
+    uint32_t par_w = 0, par_u = 0, par_b = 0;
+    uint32_t out_q = 0, par_q = 0;  // bit b: a Q+ copy into buffer b in flight / the parity of its phase
     if (warp == 0) umma::alloc(tmem_s, T_COLS);
     for (int jj = tid; jj < D; jj += NTS) nw[jj] = __ldg(a.norm_w + jj);
     if (tid == 0) {
         for (int b = 0; b < 4; ++b) mbar_init(bar_w + b, 1);
         mbar_init(bar_q, 1);
+        mbar_init(bar_q + 1, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_o + b, 1);
             mbar_init(bar_ofree + b, NOW);
@@ -1398,7 +1404,12 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             issue_qp(cb);
             issue_u(cb);
             issue_b(cb);
-            out_w = out_u = out_b = out_q = true;
+            out_w = out_u = out_b = true;
+            out_q = 1u;
+            if (cb + 1 < ce) {
+                issue_qp(cb + 1);
+                out_q = 3u;
+            }
         }
     }
     umma::fence_before();
@@ -1450,7 +1461,7 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
         umma::fence_before();
         state_sync();
         umma::fence_after();
-        uint32_t ph_w = 0, ph_u = 0, ph_b = 0, ph_m = 0, ph_q = 0;
+        uint32_t ph_w = 0, ph_u = 0, ph_b = 0, ph_m = 0;
         bool ok = true, t0ok = true;  // t0ok: thread 0's waits on the output warps' buffer releases
         // checkpoint boundaries: a running next boundary, its slot fetched one boundary ahead (no division in
         // the loop); chunk entries are fetched one chunk ahead
@@ -1525,9 +1536,11 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                                                       : 1.f;
             // ---- U^T = S^T (-W)^T.  If -W never arrives, nothing is committed and every thread's bounded wait
             //      on bar_mma gives up ----
+            // ---- U^T = S^T (-W)^T; then, once Q+ is in (copied two chunks ahead) and the output warps have read
+            //      this O^T buffer (two chunks ago), O^T = S^T Q+^T (the S^T commit below covers it).  If -W or Q+
+            //      never arrives, nothing more is committed and every thread's bounded wait on bar_mma gives up ----
             const uint32_t idp = umma::idesc(umma::kBF16, 128, CH);
             const uint64_t dS = umma::sdesc_k(Sst, D, 0);
-            bool issued = false;
             if (tid == 0 && mbar_wait(bar_w, ph_w)) {
                 out_w = false;
                 const uint64_t dW = umma::sdesc_k(ops + WS_W, CH, 0);
@@ -1535,28 +1548,23 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 for (int ks = 0; ks < D / 16; ++ks)
                     umma::mma_bf16(tmem + T_U, umma::sdesc_at(dS, D, ks), umma::sdesc_at(dW, CH, ks), idp, ks > 0);
                 umma::commit(bar_mma);
-                issued = true;
-            }
-            ph_w ^= 1;
-            // the rest of the state pass of the chunk before, while the MMAs above run: its checkpoint, and
-            // S^T diag(exp(G_last of this chunk)) back to tensor memory for this chunk's S^T MMA
-            if (c > cb) s_rest(ck_prev, gln + (c & 1) * D);
-            // ---- once Q+ is in and the output warps have read this O^T buffer (two chunks ago):
-            //      O^T = S^T Q+^T (the S^T commit below covers it) ----
-            if (tid == 0 && issued) {
-                const bool okq = mbar_wait(bar_q, ph_q);
-                if (okq) out_q = false;
+                const int qb = ob;  // (the same chunk parity)
+                const bool okq = mbar_wait(bar_q + qb, opar);
+                if (okq) out_q &= ~(1u << qb);
                 if (!okq || (c - cb >= 2 && !mbar_wait(bar_ofree + ob, opar ^ 1u))) t0ok = false;
                 umma::fence_after();
                 if (t0ok) {
                     const uint32_t tob = tmem + T_O + 64u * (uint32_t)ob;
-                    const uint64_t dQ = umma::sdesc_k(ops + WS_QP, CH, 0);
+                    const uint64_t dQ = umma::sdesc_k(qpbuf(qb), CH, 0);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
                         umma::mma_bf16(tob, umma::sdesc_at(dS, D, ks), umma::sdesc_at(dQ, CH, ks), idp, ks > 0);
                 }
             }
-            ph_q ^= 1;
+            ph_w ^= 1;
+            // the rest of the state pass of the chunk before, while the MMAs above run: its checkpoint, and
+            // S^T diag(exp(G_last of this chunk)) back to tensor memory for this chunk's S^T MMA
+            if (c > cb) s_rest(ck_prev, gln + (c & 1) * D);
             // each thread waits for U^T itself; a timed-out wait is voted on at the barrier after the U tiles
             ok = mbar_wait(bar_mma, ph_m);
             ph_m ^= 1;
@@ -1622,10 +1630,10 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, ph_m));
             ph_m ^= 1;
             umma::fence_after();
-            if (tid == 0 && ok && has_next) {  // every MMA before the S^T commit is done: Q+ is free
-                issue_qp(c + 1);
-                out_q = true;
-                par_q = ph_q;
+            if (tid == 0 && ok && c + 2 < ce) {  // every MMA before the S^T commit is done: this Q+ buffer is free
+                issue_qp(c + 2);
+                out_q |= 1u << ob;
+                par_q = (par_q & ~(1u << ob)) | ((opar ^ 1u) << ob);
             }
 
             // ---- S pass, the part the next chunk's first MMAs wait for (this thread: key channels i0 .. i0 + 63):
@@ -1668,14 +1676,16 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
             // copies still in flight into this CTA's shared memory land before it exits (short bounded waits)
             constexpr uint64_t kDrainNs = 10000000ull;
             if (out_w) mbar_wait(bar_w, par_w, kDrainNs);
-            if (out_q) mbar_wait(bar_q, par_q, kDrainNs);
+            for (int b = 0; b < 2; ++b)
+                if (out_q >> b & 1u) mbar_wait(bar_q + b, par_q >> b & 1u, kDrainNs);
             if (out_u) mbar_wait(bar_u, par_u, kDrainNs);
             if (out_b) mbar_wait(bar_b, par_b, kDrainNs);
         }
     } else {
         // ================================ output warps ================================
-        // warp ow: lane quadrant ow % 4 (NCW % 4 == 0) and token half ow / 4 of the O^T buffer when staging;
-        // tokens ow, ow + 8, ..., one warp per token, for the gated RMSNorm
+        // The O^T buffer is staged and normalised in two halves of 32 tokens.  Staging: warp ow takes lane
+        // quadrant ow % 4 (NCW % 4 == 0) and 16 tokens (ow / 4) of the half; the gated RMSNorm: tokens ow,
+        // ow + 8, ..., one warp per token
         const int ow = warp - NCW, oq = ow & 3, oh = ow >> 2;
         uint2 zr[8];
         auto fetch_gates = [&](const ChunkEnt &e) {  // the output gate of this warp's tokens of a chunk
@@ -1702,52 +1712,60 @@ __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillA
                 break;
             }
             umma::fence_after();
-            {
-                uint32_t va[32];
-                umma::ld32_issue(tmem + ((uint32_t)(32 * oq) << 16) + T_O + 64u * (uint32_t)ob + 32u * (uint32_t)oh, va);
-                umma::wait_ld(va);
-                const int jo = 32 * oq + lane;
-#pragma unroll
-                for (int t = 0; t < 32; ++t) Ost[(32 * oh + t) * OST + jo] = __uint_as_float(va[t]);
-            }
-            umma::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(bar_ofree + ob, 0);  // this warp's part of the buffer is read
-            out_sync_or(false);  // the whole O tile is staged
             const float4 w4 = *reinterpret_cast<const float4 *>(nw + 4 * lane);
-            // the 8 rows are read before any y store (the stores could otherwise be taken to alias the staging),
-            // and their reductions are interleaved
-            float4 o8[8];
-            float ss[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                o8[k] = *reinterpret_cast<const float4 *>(Ost + (ow + 8 * k) * OST + 4 * lane);
-                ss[k] = o8[k].x * o8[k].x;
-                ss[k] = fmaf(o8[k].y, o8[k].y, ss[k]);
-                ss[k] = fmaf(o8[k].z, o8[k].z, ss[k]);
-                ss[k] = fmaf(o8[k].w, o8[k].w, ss[k]);
-            }
+            for (int p = 0; p < 2; ++p) {
+                {   // tokens 32 p + 16 oh .. 32 p + 16 oh + 15 of value channels 32 oq .. 32 oq + 31
+                    uint32_t va[16];
+                    umma::ld16_issue(tmem + ((uint32_t)(32 * oq) << 16) + T_O + 64u * (uint32_t)ob + 32u * (uint32_t)p +
+                                         16u * (uint32_t)oh,
+                                     va);
+                    umma::wait_ld16(va);
+                    const int jo = 32 * oq + lane;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
+                    for (int t = 0; t < 16; ++t) Ost[(16 * oh + t) * OST + jo] = __uint_as_float(va[t]);
+                }
+                if (p == 1) {  // this warp's parts of the buffer are read
+                    umma::fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_expect_tx(bar_ofree + ob, 0);
+                }
+                out_sync_or(false);  // these 32 tokens are staged
+                // the 4 rows are read before any y store (the stores could otherwise be taken to alias the
+                // staging), and their reductions are interleaved
+                float4 o4r[4];
+                float ss[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], o);
+                for (int k = 0; k < 4; ++k) {
+                    o4r[k] = *reinterpret_cast<const float4 *>(Ost + (ow + 8 * k) * OST + 4 * lane);
+                    ss[k] = o4r[k].x * o4r[k].x;
+                    ss[k] = fmaf(o4r[k].y, o4r[k].y, ss[k]);
+                    ss[k] = fmaf(o4r[k].z, o4r[k].z, ss[k]);
+                    ss[k] = fmaf(o4r[k].w, o4r[k].w, ss[k]);
+                }
+                if (p == 0) out_sync_or(false);  // every warp has read this half before the next is staged
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int r = ow + 8 * k;
-                const float4 o4 = o8[k];
-                const float rr = rsqrtf(ss[k] * (1.0f / D) + a.rms_eps);
-                if (r < e.n) {
-                    float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
-                    if (a.z) {
-                        const uint2 zz = zr[k];
-                        y0 *= sigmoid_gate(bf2f((uint16_t)(zz.x & 0xffff)));
-                        y1 *= sigmoid_gate(bf2f((uint16_t)(zz.x >> 16)));
-                        y2 *= sigmoid_gate(bf2f((uint16_t)(zz.y & 0xffff)));
-                        y3 *= sigmoid_gate(bf2f((uint16_t)(zz.y >> 16)));
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], o);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 32 * p + ow + 8 * k;
+                    const float4 o4 = o4r[k];
+                    const float rr = rsqrtf(ss[k] * (1.0f / D) + a.rms_eps);
+                    if (r < e.n) {
+                        float y0 = o4.x * rr * w4.x, y1 = o4.y * rr * w4.y, y2 = o4.z * rr * w4.z, y3 = o4.w * rr * w4.w;
+                        if (a.z) {
+                            const uint2 zz = zr[4 * p + k];
+                            y0 *= sigmoid_gate(bf2f((uint16_t)(zz.x & 0xffff)));
+                            y1 *= sigmoid_gate(bf2f((uint16_t)(zz.x >> 16)));
+                            y2 *= sigmoid_gate(bf2f((uint16_t)(zz.y & 0xffff)));
+                            y3 *= sigmoid_gate(bf2f((uint16_t)(zz.y >> 16)));
+                        }
+                        *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
+                            make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
+                                       (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
                     }
-                    *(reinterpret_cast<uint2 *>(a.y + ((size_t)(e.t0 + r) * H + h) * D) + lane) =
-                        make_uint2((uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16),
-                                   (uint32_t)f2bf(y2) | ((uint32_t)f2bf(y3) << 16));
                 }
             }
         }
