@@ -1316,13 +1316,15 @@ __device__ __forceinline__ bool out_sync_or(bool p) {
 //   U^T  = S^T (-W)^T                 (MMA, no accumulate)
 //   U    = U' + U^T read back         -> tf32 operand tile
 //   S^T += U^T Ktil                   (MMA; S^T already holds S^T diag(exp(G_last)))
-//   S pass: bf16 operand tile of the new S, checkpoint, then S^T diag(exp(G_last of the next chunk)) back to
-//   tensor memory (or the final state to dst).
+//   S pass: the bf16 operand tile of the new S, which the next chunk's first MMAs read; then, once those are
+//   issued and while they run, the checkpoint and S^T diag(exp(G_last of the next chunk)) back to tensor
+//   memory (or the final state to dst).
 // The output MMAs O^T = S^T Q+^T + U^T Qk^T go to one of two tensor-memory buffers, which the eight output warps
-// read themselves: they apply the gated RMSNorm and store y while the chain goes on, and release the buffer for
-// the chunk after next.  Each chain warp owns one lane quadrant (32 value channels) and half of the columns:
-// 64 key channels of S, 32 tokens of U.  The chunk block arrives in three bulk copies, each issued as soon as
-// the previous chunk no longer reads its region.
+// read themselves, half a chunk at a time: they apply the gated RMSNorm and store y while the chain goes on, and
+// release the buffer for the chunk after next.  Each chain warp owns one lane quadrant (32 value channels) and
+// half of the columns: 64 key channels of S, 32 tokens of U.  The chunk block arrives in bulk copies, each
+// issued as soon as the chunk before no longer reads its region; Q+ has two buffers and is copied two chunks
+// ahead, so that the first O^T MMAs follow the U^T ones at once.
 __global__ void __launch_bounds__(NTS, 1) prefill_state_tc_kernel(const PrefillArgs a, const Layout2 L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
