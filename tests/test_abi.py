@@ -144,3 +144,27 @@ def test_check_slots_enforces_the_aliasing_contract(lib):
         with pytest.raises(kda.KdaError) as e:
             ok(*args)
         assert e.value.rc == kda.KDA_ERR_INVALID_ARG and words in str(e.value), (args, str(e.value))
+
+
+def test_noalloc_checks_arguments_then_size_before_any_device_call(lib):
+    """The no-allocation entry point's documented order: argument checks (no CUDA call), then the size check
+    against its static scratch (no CUDA call), and only then the device look-up.  On a machine without a GPU
+    the first two still answer."""
+    import hybrid_linear_attention_decode_gb300 as kda
+    prm = kda._Params(ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000), 1e-6, 1e-6, 1.0, 1)
+    pool = kda._Pool(2, 128, 128, 4, 0, 0, 8, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))
+    p16 = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(16)]  # aligned stand-ins, never dereferenced
+    # a NULL pool is an invalid argument
+    rc = lib.kda_prefill_chunked_noalloc(None, ctypes.byref(prm), 1, 64, *p16[:4], 64, 0, None, None,
+                                         *p16[4:11], None, None)
+    assert rc == kda.KDA_ERR_INVALID_ARG
+    # an interval that is not a multiple of the chunk is an invalid argument
+    rc = lib.kda_prefill_chunked_noalloc(ctypes.byref(pool), ctypes.byref(prm), 1, 64, *p16[:4], 64, 96,
+                                         p16[4], p16[5], *p16[6:13], None, None)
+    assert rc == kda.KDA_ERR_INVALID_ARG and "multiple of the chunk" in kda.kda_last_error_string()
+    # a problem whose workspace exceeds the static scratch is refused without a launch
+    tokens = 1 << 20
+    assert lib.kda_prefill_workspace_bytes(ctypes.byref(pool), 1, tokens, 64) > kda.NOALLOC_SCRATCH_BYTES
+    rc = lib.kda_prefill_chunked_noalloc(ctypes.byref(pool), ctypes.byref(prm), 1, tokens, *p16[:4], 64, 0, None,
+                                         None, *p16[4:11], None, None)
+    assert rc == kda.KDA_ERR_WORKSPACE and "static scratch" in kda.kda_last_error_string()
